@@ -1,0 +1,211 @@
+/*
+ * gemm.h -- C ABI of the GB300 (sm_103a) dense GEMM library.
+ *
+ * Computes C = A * B with fp16 or bf16 inputs, fp32 accumulation and an
+ * output of the input type, rounded once to nearest-even.  The output tiles
+ * are scheduled three ways:
+ *
+ *   GEMM_SCHED_DATA_PARALLEL  one CTA per output tile, which ends after its
+ *                             tile (HF post "naive vs persistent matmul":
+ *                             the naive tiled matmul; GitHub issue
+ *                             "Stream-k matmul implementation very slow ...",
+ *                             final version, "tile matmul (grid=0)").
+ *   GEMM_SCHED_PERSISTENT     one CTA per SM, each looping over tiles in a
+ *                             grouped raster order (HF post: persistent
+ *                             matmul; issue, final version, swizzle_tile).
+ *   GEMM_SCHED_STREAMK        hybrid Stream-K (issue, final version, wrapper
+ *                             and first_wave): the first sk tiles are split
+ *                             evenly by k-iteration over g CTAs, the rest are
+ *                             whole tiles.  Split tiles are fixed up through
+ *                             a fp32 workspace and per-tile flags, in a fixed
+ *                             order, so results are deterministic.
+ *
+ * Conventions for every entry point:
+ *  - Each call returns a gemm_status_t; nothing else crosses the ABI.  An
+ *    out-parameter is left untouched when the call fails.
+ *  - Matrices are dense.  A is M x K, B is K x N, both row- or column-major
+ *    (leading dimension K or M for A, N or K for B).  C is M x N row-major
+ *    (leading dimension N).  Elements are 16-bit (fp16 or bf16, one type for
+ *    A, B and C).
+ *  - A, B, C and the workspace are DEVICE pointers owned by the caller, on the
+ *    device that was current when the plan was created.  They must be 16-byte
+ *    aligned.  K and N must be multiples of 8; M must be one too when A is
+ *    column-major (the hardware tensor copy needs 16-byte row strides).
+ *    Otherwise gemm_run returns GEMM_ERR_UNSUPPORTED.
+ *  - gemm_run is asynchronous on the given stream.  Launch errors return at
+ *    once; a device-side wait that ran out of time is reported by
+ *    gemm_last_status.
+ *  - A plan is not thread-safe.  Two runs that share one workspace must not
+ *    overlap in time (use one stream or order them).
+ */
+#ifndef PSM_GEMM_H
+#define PSM_GEMM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { GEMM_F16 = 0, GEMM_BF16 = 1 } gemm_dtype_t;
+typedef enum { GEMM_ROW_MAJOR = 0, GEMM_COL_MAJOR = 1 } gemm_layout_t;
+typedef enum {
+    GEMM_SCHED_DATA_PARALLEL = 0,
+    GEMM_SCHED_PERSISTENT = 1,
+    GEMM_SCHED_STREAMK = 2
+} gemm_schedule_t;
+
+typedef enum {
+    GEMM_OK = 0,
+    GEMM_ERR_INVALID_ARG = 1,  /* NULL handle/pointer, negative size, bad enum or key */
+    GEMM_ERR_UNSUPPORTED = 2,  /* alignment / stride / option value not supported */
+    GEMM_ERR_WORKSPACE = 3,    /* workspace NULL or misaligned while one is needed */
+    GEMM_ERR_CUDA = 4,         /* a CUDA runtime call failed */
+    GEMM_ERR_LAUNCH = 5,       /* the kernel launch was refused (e.g. grid not co-resident) */
+    GEMM_ERR_TIMEOUT = 6,      /* a bounded device wait gave up; the tile's C was not written */
+    GEMM_ERR_NO_DEVICE = 7     /* no CUDA device, or not an sm_103 device, or an offline plan */
+} gemm_status_t;
+
+/* cudaStream_t without the CUDA headers: the same type. NULL = default stream. */
+typedef struct CUstream_st *gemm_stream_t;
+
+typedef struct gemm_plan *gemm_plan_t;
+
+/* Options for gemm_plan_set_option (key, value). */
+enum {
+    /* g: CTAs of the persistent / Stream-K grid. 0 (default) = number of SMs.
+     * Must not exceed the SM count for GEMM_SCHED_STREAMK (the CTAs wait on
+     * one another, so all must be resident at once). */
+    GEMM_OPT_GRID = 1,
+    /* rows of tiles per raster group (issue, final version, GROUP_M); 0 selects
+     * the linear raster.  Default 8 for PERSISTENT and STREAMK, 0 for
+     * DATA_PARALLEL. */
+    GEMM_OPT_GROUP_M = 2,
+    /* output tile width BN: 128 or 256; 0 (default) lets the plan choose.
+     * The tile height is 128 rows and the k-slice 64. */
+    GEMM_OPT_TILE_N = 3,
+    /* 1 (default): the issue's "two_tiles" rule adds g more Stream-K tiles
+     * when more than g whole tiles would remain; 0: sk = tiles mod g. */
+    GEMM_OPT_TWO_TILES = 4,
+    /* bound on a Stream-K owner's wait for its peers, microseconds (default
+     * 1000000).  On expiry the tile's C is not written and gemm_last_status
+     * reports GEMM_ERR_TIMEOUT. */
+    GEMM_OPT_WAIT_LIMIT_US = 5,
+    /* test hook: the CTA with this index skips posting its peer flag, so its
+     * owner's wait runs out.  -1 (default) = off. */
+    GEMM_OPT_INJECT_SKIP_POST = 6
+};
+
+/* Keys for gemm_plan_get_info. */
+enum {
+    GEMM_INFO_TILE_M = 1, GEMM_INFO_TILE_N = 2, GEMM_INFO_TILE_K = 3,
+    GEMM_INFO_TILES_M = 4, GEMM_INFO_TILES_N = 5, GEMM_INFO_TILES = 6,
+    GEMM_INFO_ITERS_PER_TILE = 7,   /* k-iterations per tile, ceil(K / 64) */
+    GEMM_INFO_GRID = 8,             /* CTAs launched by gemm_run */
+    GEMM_INFO_SK_TILES = 9,         /* tiles split by the Stream-K wave */
+    GEMM_INFO_SK_ITERS_PER_CTA = 10,/* even share of Stream-K iterations */
+    GEMM_INFO_SK_ITERS_REM = 11,    /* CTAs that take one iteration more */
+    GEMM_INFO_NUM_SMS = 12,
+    GEMM_INFO_STAGES = 13,          /* depth of the shared-memory ring */
+    GEMM_INFO_GROUP_M = 14,
+    GEMM_INFO_SMEM_BYTES = 15       /* dynamic shared memory per CTA */
+};
+
+/* Roles of a work unit reported by gemm_plan_units. */
+enum { GEMM_ROLE_FULL = 0, GEMM_ROLE_OWNER = 1, GEMM_ROLE_PEER = 2 };
+
+/*
+ * Create a plan for one problem shape on the current CUDA device.
+ * Tile grid and Stream-K split: issue, final version, wrapper (_call).
+ * M, N, K >= 0.  *out receives a handle that gemm_plan_destroy frees.
+ * Errors: INVALID_ARG (NULL out, negative size, bad enum), NO_DEVICE (no
+ * device, or the device is not compute capability 10.3), CUDA.
+ */
+gemm_status_t gemm_plan_create(gemm_plan_t *out, int64_t M, int64_t N, int64_t K,
+                               gemm_dtype_t dtype, gemm_layout_t layout_a,
+                               gemm_layout_t layout_b, gemm_schedule_t schedule);
+
+/*
+ * Same as gemm_plan_create but touches no device: a plan for inspection only
+ * (gemm_plan_get_info, gemm_plan_units, gemm_workspace_size) as if the device
+ * had num_sms SMs.  gemm_run on it returns GEMM_ERR_NO_DEVICE.
+ */
+gemm_status_t gemm_plan_create_offline(gemm_plan_t *out, int64_t M, int64_t N, int64_t K,
+                                       gemm_dtype_t dtype, gemm_layout_t layout_a,
+                                       gemm_layout_t layout_b, gemm_schedule_t schedule,
+                                       int num_sms);
+
+/* Set one GEMM_OPT_* option; the plan is re-derived.  Errors: INVALID_ARG
+ * (NULL plan, unknown key), UNSUPPORTED (value out of range). */
+gemm_status_t gemm_plan_set_option(gemm_plan_t plan, int key, int64_t value);
+
+/* Read one GEMM_INFO_* value into *value.  Errors: INVALID_ARG. */
+gemm_status_t gemm_plan_get_info(gemm_plan_t plan, int key, int64_t *value);
+
+/*
+ * Bytes of device workspace gemm_run needs: 0 for DATA_PARALLEL and
+ * PERSISTENT; for STREAMK, 8 bytes of flag per split tile (rounded up to 256)
+ * plus one 128 x BN fp32 partial-tile slot per CTA (the "scratchpad" of the
+ * Stream-K fixup mentioned in the issue, second code version).
+ * The caller allocates it (16-byte aligned) and owns it; the plan clears the
+ * flag part the first time it sees a workspace address.  Errors: INVALID_ARG.
+ */
+gemm_status_t gemm_workspace_size(gemm_plan_t plan, size_t *bytes);
+
+/*
+ * C = A * B on `stream`, asynchronously.  `workspace` may be NULL only when
+ * gemm_workspace_size is 0.  C is written in full (every element, once);
+ * A and B are only read.  M == 0 or N == 0: nothing is done.  K == 0: C is
+ * set to +0.
+ * Errors: INVALID_ARG (NULL plan or operand), UNSUPPORTED (alignment),
+ * WORKSPACE, NO_DEVICE (offline plan), CUDA, LAUNCH.
+ */
+gemm_status_t gemm_run(gemm_plan_t plan, const void *A, const void *B, void *C,
+                       void *workspace, gemm_stream_t stream);
+
+/*
+ * End-to-end variant: copies hA -> dA and hB -> dB (host to device), runs
+ * gemm_run(dA, dB, dC), and copies dC -> hC (device to host), all enqueued on
+ * `stream`.  Host buffers should be pinned for the copies to be asynchronous.
+ * The caller owns all six buffers; nothing is allocated.  Errors: as gemm_run.
+ */
+gemm_status_t gemm_run_host(gemm_plan_t plan, const void *hA, const void *hB, void *hC,
+                            void *dA, void *dB, void *dC, void *workspace,
+                            gemm_stream_t stream);
+
+/*
+ * Synchronise `stream`, then read and clear the plan's device status word.
+ * Returns GEMM_OK, GEMM_ERR_TIMEOUT (a bounded device wait expired since the
+ * last call), or GEMM_ERR_CUDA (the stream reported an error).
+ */
+gemm_status_t gemm_last_status(gemm_plan_t plan, gemm_stream_t stream);
+
+/*
+ * Host twin of the device tile scheduler: the work units CTA `cta` executes,
+ * in order, 5 int32 per unit: tile id (raster order), first k-iteration,
+ * end k-iteration, role (GEMM_ROLE_*), peers (for an OWNER: how many peer
+ * partials it adds; else 0).  Writes at most max_units units to `units`
+ * (may be NULL when max_units is 0) and the full count to *n_units.
+ * Segments: issue, final version, first_wave (the range of a program cut at
+ * tile boundaries) and full_tiles.  Errors: INVALID_ARG.
+ */
+gemm_status_t gemm_plan_units(gemm_plan_t plan, int64_t cta, int32_t *units,
+                              int64_t max_units, int64_t *n_units);
+
+/* Tile coordinates (tile row, tile column) of raster id `tile` (issue, final
+ * version, swizzle_tile / linear_tile).  Errors: INVALID_ARG. */
+gemm_status_t gemm_plan_tile_coords(gemm_plan_t plan, int64_t tile, int64_t *tile_m,
+                                    int64_t *tile_n);
+
+/* Free the plan and its device status word.  NULL is accepted. */
+gemm_status_t gemm_plan_destroy(gemm_plan_t plan);
+
+/* Static text for a status code (never NULL). */
+const char *gemm_status_string(gemm_status_t status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PSM_GEMM_H */

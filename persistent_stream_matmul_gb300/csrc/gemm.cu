@@ -1,0 +1,541 @@
+// Host side of the GEMM library: plans, tensor-map encoding, launches and the
+// C ABI declared in include/gemm.h.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <new>
+
+#include "gemm.h"
+#include "gemm_kernel.cuh"
+
+using namespace psm;
+
+namespace {
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// Run numbers tagged into the Stream-K flags.  Global so that plans sharing
+// one workspace never reuse a number; 0 is never handed out, so a zeroed flag
+// matches no run.
+std::atomic<uint32_t> g_epoch{0x1000u};
+
+uint32_t next_epoch() {
+    uint32_t e;
+    do { e = ++g_epoch; } while (e == 0);
+    return e;
+}
+
+int64_t cdiv64(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+}  // namespace
+
+struct gemm_plan {
+    int64_t M, N, K;
+    int dtype, layout_a, layout_b, schedule;
+    int device, num_sms, offline;
+    // options
+    int opt_grid, opt_group_m, opt_tile_n, opt_two_tiles, inject_skip;
+    int64_t wait_limit_us;
+    // derived
+    int BN, stages, smem_bytes;
+    Sched s;
+    size_t ws_flag_bytes, ws_bytes;
+    // device state
+    int* d_status;
+    // caches
+    const void* tm_a_ptr;
+    const void* tm_b_ptr;
+    bool tm_valid;
+    CUtensorMap tmA, tmB;
+    const void* flags_cleared_for;
+    bool attr_set[2];
+};
+
+namespace {
+
+bool valid_enums(int dtype, int la, int lb, int sched) {
+    return (dtype == GEMM_F16 || dtype == GEMM_BF16) && (la == 0 || la == 1) &&
+           (lb == 0 || lb == 1) && (sched >= 0 && sched <= 2);
+}
+
+template <int BN, bool BF>
+void* kernel_ptr() {
+    return reinterpret_cast<void*>(&gemm_kernel<BN, BF>);
+}
+
+void* pick_kernel(int BN, int dtype) {
+    if (BN == 256) return dtype == GEMM_BF16 ? kernel_ptr<256, true>() : kernel_ptr<256, false>();
+    return dtype == GEMM_BF16 ? kernel_ptr<128, true>() : kernel_ptr<128, false>();
+}
+
+int smem_for(int BN) { return BN == 256 ? Cfg<256>::SMEM_BYTES : Cfg<128>::SMEM_BYTES; }
+int stages_for(int BN) { return BN == 256 ? Cfg<256>::STAGES : Cfg<128>::STAGES; }
+
+// Derive the tile grid and the schedule from the shape and the options
+// (issue "Stream-k matmul implementation very slow ...", final version,
+// wrapper: tile counts, Stream-K tile count with the two_tiles rule, even
+// split of the Stream-K iterations).
+gemm_status_t derive(gemm_plan* p) {
+    const int64_t tiles_m = cdiv64(p->M, BM);
+    int BN = p->opt_tile_n;
+    if (BN == 0) {
+        const int64_t tiles256 = tiles_m * cdiv64(p->N, 256);
+        BN = (p->N > 128 && tiles256 >= p->num_sms) ? 256 : 128;
+    }
+    const int64_t tiles_n = cdiv64(p->N, BN);
+    const int64_t tiles = tiles_m * tiles_n;
+    const int64_t ipt = cdiv64(p->K, BK);
+    if (tiles > INT32_MAX / 2 || ipt > INT32_MAX / 2) return GEMM_ERR_UNSUPPORTED;
+
+    Sched s{};
+    s.tiles_m = (int32_t)tiles_m;
+    s.tiles_n = (int32_t)tiles_n;
+    s.tiles = (int32_t)tiles;
+    s.ipt = (int32_t)(ipt > 0 ? ipt : 1);
+    s.group_m = p->opt_group_m >= 0 ? p->opt_group_m
+                                    : (p->schedule == GEMM_SCHED_DATA_PARALLEL ? 0 : 8);
+    const int g = p->opt_grid > 0 ? p->opt_grid : p->num_sms;
+    s.sk_tiles = 0;
+    s.sk_q = s.sk_r = 0;
+    if (p->schedule == GEMM_SCHED_DATA_PARALLEL) {
+        s.grid = s.tiles;
+        s.persistent = 0;
+    } else if (p->schedule == GEMM_SCHED_PERSISTENT) {
+        s.grid = (int32_t)(tiles < g ? tiles : g);
+        s.persistent = 1;
+    } else {
+        int64_t sk = tiles % g;
+        if (p->opt_two_tiles && tiles - sk > g) sk += g;
+        s.sk_tiles = (int32_t)sk;
+        s.grid = tiles > 0 ? g : 0;
+        s.persistent = 1;
+        const int64_t iters = sk * (int64_t)s.ipt;
+        s.sk_q = iters / g;
+        s.sk_r = iters % g;
+    }
+    p->s = s;
+    p->BN = BN;
+    p->stages = stages_for(BN);
+    p->smem_bytes = smem_for(BN);
+    if (p->schedule == GEMM_SCHED_STREAMK && s.sk_tiles > 0) {
+        p->ws_flag_bytes = ((size_t)s.sk_tiles * 8 + 255) / 256 * 256;
+        p->ws_bytes = p->ws_flag_bytes + (size_t)s.grid * BM * BN * sizeof(float);
+    } else {
+        p->ws_flag_bytes = 0;
+        p->ws_bytes = 0;
+    }
+    p->tm_valid = false;
+    return GEMM_OK;
+}
+
+gemm_status_t make_plan(gemm_plan_t* out, int64_t M, int64_t N, int64_t K, int dtype, int la,
+                        int lb, int sched, int offline, int num_sms) {
+    if (!out || M < 0 || N < 0 || K < 0 || !valid_enums(dtype, la, lb, sched))
+        return GEMM_ERR_INVALID_ARG;
+    gemm_plan* p = new (std::nothrow) gemm_plan();
+    if (!p) return GEMM_ERR_CUDA;
+    p->M = M;
+    p->N = N;
+    p->K = K;
+    p->dtype = dtype;
+    p->layout_a = la;
+    p->layout_b = lb;
+    p->schedule = sched;
+    p->offline = offline;
+    p->opt_grid = 0;
+    p->opt_group_m = -1;
+    p->opt_tile_n = 0;
+    p->opt_two_tiles = 1;
+    p->inject_skip = -1;
+    p->wait_limit_us = 1000000;
+    if (offline) {
+        if (num_sms <= 0) { delete p; return GEMM_ERR_INVALID_ARG; }
+        p->device = -1;
+        p->num_sms = num_sms;
+    } else {
+        int dev = 0, count = 0;
+        if (cudaGetDeviceCount(&count) != cudaSuccess || count == 0) {
+            cudaGetLastError();
+            delete p;
+            return GEMM_ERR_NO_DEVICE;
+        }
+        int major = 0, minor = 0, sms = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+            delete p;
+            return GEMM_ERR_CUDA;
+        }
+        if (major != 10 || minor != 3) { delete p; return GEMM_ERR_NO_DEVICE; }
+        p->device = dev;
+        p->num_sms = sms;
+        if (cudaMalloc(&p->d_status, sizeof(int)) != cudaSuccess ||
+            cudaMemset(p->d_status, 0, sizeof(int)) != cudaSuccess) {
+            if (p->d_status) cudaFree(p->d_status);
+            delete p;
+            return GEMM_ERR_CUDA;
+        }
+    }
+    gemm_status_t st = derive(p);
+    if (st != GEMM_OK) {
+        if (p->d_status) cudaFree(p->d_status);
+        delete p;
+        return st;
+    }
+    if (getenv("GEMM_DEBUG")) {
+        fprintf(stderr,
+                "[gemm] M=%lld N=%lld K=%lld dtype=%d A=%s B=%s sched=%d | tile 128x%dx64 "
+                "tiles %dx%d=%d ipt=%d grid=%d sk_tiles=%d sk_q=%lld sk_r=%lld group_m=%d "
+                "ws=%zu smem=%d\n",
+                (long long)M, (long long)N, (long long)K, dtype, la ? "col" : "row",
+                lb ? "col" : "row", sched, p->BN, p->s.tiles_m, p->s.tiles_n, p->s.tiles,
+                p->s.ipt, p->s.grid, p->s.sk_tiles, (long long)p->s.sk_q, (long long)p->s.sk_r,
+                p->s.group_m, p->ws_bytes, p->smem_bytes);
+    }
+    *out = p;
+    return GEMM_OK;
+}
+
+gemm_status_t encode_maps(gemm_plan* p, const void* A, const void* B) {
+    if (p->tm_valid && p->tm_a_ptr == A && p->tm_b_ptr == B) return GEMM_OK;
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return GEMM_ERR_CUDA;
+    const CUtensorMapDataType dt =
+        p->dtype == GEMM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    const cuuint32_t estr[2] = {1, 1};
+    // A: row-major M x K -> dims {K, M}, box {64, 128}; column-major -> dims {M, K}, box {64, 64}
+    {
+        cuuint64_t dims[2], strides[1];
+        cuuint32_t box[2];
+        if (p->layout_a == GEMM_ROW_MAJOR) {
+            dims[0] = (cuuint64_t)p->K; dims[1] = (cuuint64_t)p->M;
+            strides[0] = (cuuint64_t)p->K * 2;
+            box[0] = BK; box[1] = BM;
+        } else {
+            dims[0] = (cuuint64_t)p->M; dims[1] = (cuuint64_t)p->K;
+            strides[0] = (cuuint64_t)p->M * 2;
+            box[0] = 64; box[1] = BK;
+        }
+        if (enc(&p->tmA, dt, 2, const_cast<void*>(A), dims, strides, box, estr,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return GEMM_ERR_UNSUPPORTED;
+    }
+    // B: column-major K x N (stored N x K) -> dims {K, N}, box {64, BN};
+    //    row-major K x N -> dims {N, K}, box {64, 64}
+    {
+        cuuint64_t dims[2], strides[1];
+        cuuint32_t box[2];
+        if (p->layout_b == GEMM_COL_MAJOR) {
+            dims[0] = (cuuint64_t)p->K; dims[1] = (cuuint64_t)p->N;
+            strides[0] = (cuuint64_t)p->K * 2;
+            box[0] = BK; box[1] = (cuuint32_t)p->BN;
+        } else {
+            dims[0] = (cuuint64_t)p->N; dims[1] = (cuuint64_t)p->K;
+            strides[0] = (cuuint64_t)p->N * 2;
+            box[0] = 64; box[1] = BK;
+        }
+        if (enc(&p->tmB, dt, 2, const_cast<void*>(B), dims, strides, box, estr,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return GEMM_ERR_UNSUPPORTED;
+    }
+    p->tm_a_ptr = A;
+    p->tm_b_ptr = B;
+    p->tm_valid = true;
+    return GEMM_OK;
+}
+
+struct DeviceGuard {
+    int prev = -1;
+    bool ok = true;
+    explicit DeviceGuard(int dev) {
+        if (cudaGetDevice(&prev) != cudaSuccess) { ok = false; return; }
+        if (prev != dev && cudaSetDevice(dev) != cudaSuccess) ok = false;
+    }
+    ~DeviceGuard() {
+        int cur = -1;
+        if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
+    }
+};
+
+}  // namespace
+
+extern "C" {
+
+gemm_status_t gemm_plan_create(gemm_plan_t* out, int64_t M, int64_t N, int64_t K,
+                               gemm_dtype_t dtype, gemm_layout_t layout_a, gemm_layout_t layout_b,
+                               gemm_schedule_t schedule) {
+    return make_plan(out, M, N, K, dtype, layout_a, layout_b, schedule, 0, 0);
+}
+
+gemm_status_t gemm_plan_create_offline(gemm_plan_t* out, int64_t M, int64_t N, int64_t K,
+                                       gemm_dtype_t dtype, gemm_layout_t layout_a,
+                                       gemm_layout_t layout_b, gemm_schedule_t schedule,
+                                       int num_sms) {
+    return make_plan(out, M, N, K, dtype, layout_a, layout_b, schedule, 1, num_sms);
+}
+
+gemm_status_t gemm_plan_set_option(gemm_plan_t p, int key, int64_t value) {
+    if (!p) return GEMM_ERR_INVALID_ARG;
+    gemm_plan saved = *p;
+    switch (key) {
+        case GEMM_OPT_GRID:
+            if (value < 0 || value > 65535) return GEMM_ERR_UNSUPPORTED;
+            if (p->schedule == GEMM_SCHED_STREAMK && value > p->num_sms) return GEMM_ERR_UNSUPPORTED;
+            p->opt_grid = (int)value;
+            break;
+        case GEMM_OPT_GROUP_M:
+            if (value < 0 || value > 4096) return GEMM_ERR_UNSUPPORTED;
+            p->opt_group_m = (int)value;
+            break;
+        case GEMM_OPT_TILE_N:
+            if (value != 0 && value != 128 && value != 256) return GEMM_ERR_UNSUPPORTED;
+            p->opt_tile_n = (int)value;
+            break;
+        case GEMM_OPT_TWO_TILES:
+            if (value != 0 && value != 1) return GEMM_ERR_UNSUPPORTED;
+            p->opt_two_tiles = (int)value;
+            break;
+        case GEMM_OPT_WAIT_LIMIT_US:
+            if (value < 1 || value > 60000000) return GEMM_ERR_UNSUPPORTED;
+            p->wait_limit_us = value;
+            return GEMM_OK;
+        case GEMM_OPT_INJECT_SKIP_POST:
+            if (value < -1 || value > 65535) return GEMM_ERR_UNSUPPORTED;
+            p->inject_skip = (int)value;
+            return GEMM_OK;
+        default:
+            return GEMM_ERR_INVALID_ARG;
+    }
+    gemm_status_t st = derive(p);
+    if (st != GEMM_OK) *p = saved;
+    return st;
+}
+
+gemm_status_t gemm_plan_get_info(gemm_plan_t p, int key, int64_t* value) {
+    if (!p || !value) return GEMM_ERR_INVALID_ARG;
+    int64_t v;
+    switch (key) {
+        case GEMM_INFO_TILE_M: v = BM; break;
+        case GEMM_INFO_TILE_N: v = p->BN; break;
+        case GEMM_INFO_TILE_K: v = BK; break;
+        case GEMM_INFO_TILES_M: v = p->s.tiles_m; break;
+        case GEMM_INFO_TILES_N: v = p->s.tiles_n; break;
+        case GEMM_INFO_TILES: v = p->s.tiles; break;
+        case GEMM_INFO_ITERS_PER_TILE: v = cdiv64(p->K, BK); break;
+        case GEMM_INFO_GRID: v = p->s.grid; break;
+        case GEMM_INFO_SK_TILES: v = p->s.sk_tiles; break;
+        case GEMM_INFO_SK_ITERS_PER_CTA: v = p->s.sk_q; break;
+        case GEMM_INFO_SK_ITERS_REM: v = p->s.sk_r; break;
+        case GEMM_INFO_NUM_SMS: v = p->num_sms; break;
+        case GEMM_INFO_STAGES: v = p->stages; break;
+        case GEMM_INFO_GROUP_M: v = p->s.group_m; break;
+        case GEMM_INFO_SMEM_BYTES: v = p->smem_bytes; break;
+        default: return GEMM_ERR_INVALID_ARG;
+    }
+    *value = v;
+    return GEMM_OK;
+}
+
+gemm_status_t gemm_workspace_size(gemm_plan_t p, size_t* bytes) {
+    if (!p || !bytes) return GEMM_ERR_INVALID_ARG;
+    *bytes = p->ws_bytes;
+    return GEMM_OK;
+}
+
+gemm_status_t gemm_run(gemm_plan_t p, const void* A, const void* B, void* C, void* workspace,
+                       gemm_stream_t stream) {
+    if (!p) return GEMM_ERR_INVALID_ARG;
+    if (p->offline) return GEMM_ERR_NO_DEVICE;
+    if (p->M == 0 || p->N == 0) return GEMM_OK;
+    if (!C) return GEMM_ERR_INVALID_ARG;
+    if (((uintptr_t)C & 15u) || (p->N % 8)) return GEMM_ERR_UNSUPPORTED;
+    DeviceGuard guard(p->device);
+    if (!guard.ok) return GEMM_ERR_CUDA;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (p->K == 0) {  // empty sum: C = +0
+        return cudaMemsetAsync(C, 0, (size_t)p->M * p->N * 2, st) == cudaSuccess ? GEMM_OK
+                                                                                 : GEMM_ERR_CUDA;
+    }
+    if (!A || !B) return GEMM_ERR_INVALID_ARG;
+    if (((uintptr_t)A & 15u) || ((uintptr_t)B & 15u) || (p->K % 8) ||
+        (p->layout_a == GEMM_COL_MAJOR && (p->M % 8)))
+        return GEMM_ERR_UNSUPPORTED;
+    if (p->ws_bytes > 0 && (!workspace || ((uintptr_t)workspace & 15u))) return GEMM_ERR_WORKSPACE;
+
+    gemm_status_t es = encode_maps(p, A, B);
+    if (es != GEMM_OK) return es;
+
+    void* fn = pick_kernel(p->BN, p->dtype);
+    const int bi = p->BN == 256 ? 1 : 0;
+    if (!p->attr_set[bi]) {
+        if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, p->smem_bytes) !=
+            cudaSuccess)
+            return GEMM_ERR_CUDA;
+        p->attr_set[bi] = true;
+    }
+    if (p->ws_bytes > 0 && p->flags_cleared_for != workspace) {
+        if (cudaMemsetAsync(workspace, 0, p->ws_flag_bytes, st) != cudaSuccess) return GEMM_ERR_CUDA;
+        p->flags_cleared_for = workspace;
+    }
+
+    KParams kp{};
+    kp.s = p->s;
+    kp.M = (int32_t)p->M;
+    kp.N = (int32_t)p->N;
+    kp.K = (int32_t)p->K;
+    kp.C = C;
+    kp.flags = p->ws_bytes ? reinterpret_cast<unsigned long long*>(workspace) : nullptr;
+    kp.partials = p->ws_bytes
+                      ? reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(workspace) + p->ws_flag_bytes)
+                      : nullptr;
+    kp.status = p->d_status;
+    kp.idesc = idesc_f16(p->dtype == GEMM_BF16, p->layout_a == GEMM_COL_MAJOR,
+                         p->layout_b == GEMM_ROW_MAJOR, BM, p->BN);
+    kp.epoch = next_epoch();
+    kp.a_mn = p->layout_a == GEMM_COL_MAJOR;
+    kp.b_mn = p->layout_b == GEMM_ROW_MAJOR;
+    kp.inject_skip_cta = p->inject_skip;
+    kp.wait_limit_ns = (uint64_t)p->wait_limit_us * 1000ull;
+    kp.pipe_limit_ns = 4000000000ull;
+
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3((unsigned)p->s.grid, 1, 1);
+    cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = (size_t)p->smem_bytes;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    if (p->schedule == GEMM_SCHED_STREAMK) {
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    void* args[3] = {&p->tmA, &p->tmB, &kp};
+    cudaError_t e = cudaLaunchKernelExC(&cfg, fn, args);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_LAUNCH;
+    }
+    return GEMM_OK;
+}
+
+gemm_status_t gemm_run_host(gemm_plan_t p, const void* hA, const void* hB, void* hC, void* dA,
+                            void* dB, void* dC, void* workspace, gemm_stream_t stream) {
+    if (!p) return GEMM_ERR_INVALID_ARG;
+    if (p->offline) return GEMM_ERR_NO_DEVICE;
+    if (p->M == 0 || p->N == 0) return GEMM_OK;
+    if (!hC || !dC || (p->K > 0 && (!hA || !hB || !dA || !dB))) return GEMM_ERR_INVALID_ARG;
+    DeviceGuard guard(p->device);
+    if (!guard.ok) return GEMM_ERR_CUDA;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const size_t a_bytes = (size_t)p->M * p->K * 2, b_bytes = (size_t)p->K * p->N * 2;
+    const size_t c_bytes = (size_t)p->M * p->N * 2;
+    if (p->K > 0) {
+        if (cudaMemcpyAsync(dA, hA, a_bytes, cudaMemcpyHostToDevice, st) != cudaSuccess ||
+            cudaMemcpyAsync(dB, hB, b_bytes, cudaMemcpyHostToDevice, st) != cudaSuccess)
+            return GEMM_ERR_CUDA;
+    }
+    gemm_status_t r = gemm_run(p, dA, dB, dC, workspace, stream);
+    if (r != GEMM_OK) return r;
+    if (cudaMemcpyAsync(hC, dC, c_bytes, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+        return GEMM_ERR_CUDA;
+    return GEMM_OK;
+}
+
+gemm_status_t gemm_last_status(gemm_plan_t p, gemm_stream_t stream) {
+    if (!p) return GEMM_ERR_INVALID_ARG;
+    if (p->offline) return GEMM_ERR_NO_DEVICE;
+    DeviceGuard guard(p->device);
+    if (!guard.ok) return GEMM_ERR_CUDA;
+    if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return GEMM_ERR_CUDA;
+    int h = 0;
+    if (cudaMemcpy(&h, p->d_status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return GEMM_ERR_CUDA;
+    if (h != STATUS_OK) {
+        if (cudaMemset(p->d_status, 0, sizeof(int)) != cudaSuccess) return GEMM_ERR_CUDA;
+        return GEMM_ERR_TIMEOUT;
+    }
+    return GEMM_OK;
+}
+
+gemm_status_t gemm_plan_units(gemm_plan_t p, int64_t cta, int32_t* units, int64_t max_units,
+                              int64_t* n_units) {
+    if (!p || !n_units || cta < 0 || cta >= p->s.grid || max_units < 0 ||
+        (max_units > 0 && !units))
+        return GEMM_ERR_INVALID_ARG;
+    Cursor cur;
+    cursor_init(p->s, (int32_t)cta, cur);
+    Unit u;
+    int64_t n = 0;
+    while (cursor_next(p->s, (int32_t)cta, cur, u)) {
+        if (n < max_units) {
+            int32_t* o = units + 5 * n;
+            o[0] = u.tile;
+            o[1] = u.k0;
+            o[2] = u.k1;
+            o[3] = u.role;
+            o[4] = u.npeers;
+        }
+        ++n;
+    }
+    *n_units = n;
+    return GEMM_OK;
+}
+
+gemm_status_t gemm_plan_tile_coords(gemm_plan_t p, int64_t tile, int64_t* tile_m, int64_t* tile_n) {
+    if (!p || !tile_m || !tile_n || tile < 0 || tile >= p->s.tiles) return GEMM_ERR_INVALID_ARG;
+    int32_t tm, tn;
+    tile_coords(p->s, (int32_t)tile, tm, tn);
+    *tile_m = tm;
+    *tile_n = tn;
+    return GEMM_OK;
+}
+
+gemm_status_t gemm_plan_destroy(gemm_plan_t p) {
+    if (!p) return GEMM_OK;
+    if (p->d_status) cudaFree(p->d_status);
+    delete p;
+    return GEMM_OK;
+}
+
+const char* gemm_status_string(gemm_status_t s) {
+    switch (s) {
+        case GEMM_OK: return "GEMM_OK";
+        case GEMM_ERR_INVALID_ARG: return "GEMM_ERR_INVALID_ARG: invalid argument";
+        case GEMM_ERR_UNSUPPORTED: return "GEMM_ERR_UNSUPPORTED: alignment, stride or option not supported";
+        case GEMM_ERR_WORKSPACE: return "GEMM_ERR_WORKSPACE: workspace missing or misaligned";
+        case GEMM_ERR_CUDA: return "GEMM_ERR_CUDA: a CUDA runtime call failed";
+        case GEMM_ERR_LAUNCH: return "GEMM_ERR_LAUNCH: kernel launch refused";
+        case GEMM_ERR_TIMEOUT: return "GEMM_ERR_TIMEOUT: a bounded device wait expired";
+        case GEMM_ERR_NO_DEVICE: return "GEMM_ERR_NO_DEVICE: no sm_103 device for this plan";
+    }
+    return "GEMM_ERR_UNKNOWN";
+}
+
+}  // extern "C"

@@ -1,0 +1,409 @@
+// sm_103a GEMM kernel: C = A * B, fp16/bf16 in, fp32 accumulation in tensor
+// memory, fp16/bf16 out.  One kernel serves the data-parallel, persistent and
+// Stream-K schedules; the tile scheduler (sched.cuh) tells every CTA which
+// work units (tile, k-range, role) it runs.
+//
+// Warp roles (192 threads, one CTA per SM):
+//   warp 0      TMA producer: one lane fills a STAGES-deep ring of A/B tiles
+//               in shared memory (128-byte swizzle), guarded by full/empty
+//               mbarriers.
+//   warp 1      allocates tensor memory (two accumulators of 128 x BN fp32);
+//               one lane issues tcgen05.mma (128 x BN x 16 each) and commits
+//               to the ring's empty barriers and to the accumulator barriers.
+//   warps 2-5   epilogue: drain an accumulator (tcgen05.ld) while the MMA
+//               fills the other one.  FULL unit: round once to the output
+//               type and store C with 16-byte vector stores.  PEER unit
+//               (Stream-K, not holding k-iteration 0): store the fp32 partial
+//               to this CTA's workspace slot, then post the tile's flag.
+//               OWNER unit (holds k-iteration 0): wait until all the tile's
+//               peers have posted, add their partials in ascending k, round
+//               once, store C.
+//
+// Sources: the HF post "naive vs persistent matmul" (tile per thread-block,
+// persistent thread-blocks, warp specialisation and double buffering named
+// as the tricks that reach peak); the GitHub issue "Stream-k matmul
+// implementation very slow ..." (the Stream-K split and the fixup, whose
+// "scratchpad + barrier" form is used here instead of atomic adds).
+//
+// Every wait is bounded: a pipeline wait that runs out sets the CTA's abort
+// flag and the device status word, and all roles leave their loops; an owner
+// whose peers do not post in time skips the tile's store and records a
+// timeout.  Nothing traps.
+#pragma once
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "ptx.cuh"
+#include "sched.cuh"
+
+namespace psm {
+
+constexpr int BM = 128;              // tile rows (TMEM lanes)
+constexpr int BK = 64;               // k-slice: 64 x 2 B = one 128-byte swizzle row
+constexpr int UMMA_K = 16;           // k of one tcgen05.mma kind::f16
+constexpr int NUM_THREADS = 192;
+constexpr int EPI_WARP0 = 2;         // first epilogue warp
+constexpr int EPI_THREADS = 128;
+constexpr int A_STAGE_BYTES = BM * BK * 2;
+constexpr int SW_ATOM_BYTES = 1024;  // 8 rows x 128 B
+constexpr int MN_CHUNK_BYTES = 64 * BK * 2;  // one 64-element-wide MN-major box (8 KB)
+
+enum : int { STATUS_OK = 0, STATUS_FLAG_TIMEOUT = 1, STATUS_PIPE_TIMEOUT = 2 };
+enum : uint32_t { BAR_EPI_SYNC = 1, BAR_EPI_VOTE = 2 };  // named barriers (0 = __syncthreads)
+
+template <int BN>
+struct Cfg {
+    static constexpr int B_STAGE_BYTES = BN * BK * 2;
+    static constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
+    static constexpr int STAGES = BN == 256 ? 4 : 6;
+    static constexpr int TMEM_COLS = 2 * BN;  // two accumulators; 256 or 512
+    static constexpr int BAR_BYTES = 256;
+    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + BAR_BYTES + 1024;
+    static_assert(BN == 128 || BN == 256, "tile width");
+    static_assert((2 * STAGES + 5) * 8 + 8 <= BAR_BYTES, "barrier area");
+};
+
+struct KParams {
+    Sched s;
+    int32_t M, N, K;
+    void* C;
+    float* partials;             // Stream-K: grid slots of BM x BN fp32
+    unsigned long long* flags;   // Stream-K: one flag per split tile
+    int* status;                 // device status word (first error wins)
+    uint32_t idesc;
+    uint32_t epoch;              // run number tagged into the flags
+    int32_t a_mn, b_mn;          // operand major-ness: 0 = K-major, 1 = MN-major
+    int32_t inject_skip_cta;     // test hook, -1 = off
+    uint64_t wait_limit_ns;      // owner's wait for its peers
+    uint64_t pipe_limit_ns;      // any wait inside the CTA's own pipeline
+};
+
+__device__ __forceinline__ void record_status(int* status, int code) {
+    atomicCAS(status, 0, code);
+}
+
+// Post one peer contribution to a split tile's flag.  The flag holds
+// (epoch << 32) | posts; a value from an older run is restarted at 1.
+__device__ __forceinline__ void post_flag(unsigned long long* f, uint32_t epoch) {
+    uint64_t cur = *reinterpret_cast<volatile unsigned long long*>(f);
+#pragma unroll 1
+    for (int tries = 0; tries < (1 << 20); ++tries) {
+        uint64_t want = ((uint32_t)(cur >> 32) == epoch) ? cur + 1
+                                                         : (((uint64_t)epoch << 32) | 1ull);
+        uint64_t prev = atom_cas_release_u64(f, cur, want);
+        if (prev == cur) return;
+        cur = prev;
+    }
+}
+
+__device__ __forceinline__ bool wait_flag(const unsigned long long* f, uint64_t target,
+                                          uint64_t limit_ns) {
+    if (ld_acquire_u64(f) == target) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+#pragma unroll 1
+        for (int i = 0; i < 16; ++i) {
+            if (ld_acquire_u64(f) == target) return true;
+            __nanosleep(32);
+        }
+        if (globaltimer_ns() - t0 > limit_ns) return false;
+    }
+}
+
+// AND of a predicate over the 128 epilogue threads.
+__device__ __forceinline__ bool epi_vote_all(bool v) {
+    uint32_t out;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.and.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(out)
+        : "r"((uint32_t)v), "r"((uint32_t)BAR_EPI_VOTE), "r"((uint32_t)EPI_THREADS)
+        : "memory");
+    return out != 0;
+}
+
+template <bool OUT_BF16>
+__device__ __forceinline__ uint32_t pack2(float a, float b) {
+    if constexpr (OUT_BF16) {
+        __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+        return *reinterpret_cast<uint32_t*>(&h);
+    } else {
+        __half2 h = __floats2half2_rn(a, b);
+        return *reinterpret_cast<uint32_t*>(&h);
+    }
+}
+
+template <int BN, bool OUT_BF16>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                const __grid_constant__ KParams p) {
+    using Cf = Cfg<BN>;
+    constexpr int STAGES = Cf::STAGES;
+    extern __shared__ uint8_t smem_raw[];
+
+    // 1024-byte aligned base: the 128-byte swizzle pattern repeats every 1 KB
+    const uint32_t raw = smem_addr(smem_raw);
+    const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
+    const uint32_t sbase = raw + pad;
+    uint8_t* bar_area = smem_raw + pad + STAGES * Cf::STAGE_BYTES;
+    const uint32_t bar_base = sbase + STAGES * Cf::STAGE_BYTES;
+    auto full_bar = [&](int s) { return bar_base + 8u * s; };
+    auto empty_bar = [&](int s) { return bar_base + 8u * (STAGES + s); };
+    auto tfull_bar = [&](int b) { return bar_base + 8u * (2 * STAGES + b); };
+    auto tempty_bar = [&](int b) { return bar_base + 8u * (2 * STAGES + 2 + b); };
+    const uint32_t done_bar = bar_base + 8u * (2 * STAGES + 4);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_area + 8 * (2 * STAGES + 5));
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(bar_area + 8 * (2 * STAGES + 5) + 4);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int cta = blockIdx.x;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(tfull_bar(b), 1);
+            mbar_init(tempty_bar(b), EPI_THREADS / 32);
+        }
+        mbar_init(done_bar, 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_addr(tmem_slot), Cf::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem_base = *tmem_slot;
+
+    auto fail_pipe = [&]() {
+        *abort_flag = 1;
+        record_status(p.status, STATUS_PIPE_TIMEOUT);
+    };
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            const uint64_t policy = l2_policy_evict_normal();
+            Cursor cur;
+            cursor_init(p.s, cta, cur);
+            Unit u;
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t filled = 0, fill_parity = 0;  // per-stage bit masks
+            bool ok = true;
+            while (ok && cursor_next(p.s, cta, cur, u)) {
+                const int m0 = u.tm * BM, n0 = u.tn * BN;
+                for (int kb = u.k0; kb < u.k1; ++kb) {
+                    if (!mbar_wait(empty_bar(stage), phase ^ 1u, p.pipe_limit_ns)) {
+                        fail_pipe();
+                        ok = false;
+                        break;
+                    }
+                    if (*abort_flag) { ok = false; break; }
+                    const uint32_t fb = full_bar(stage);
+                    const uint32_t sa = sbase + stage * Cf::STAGE_BYTES;
+                    const uint32_t sb = sa + A_STAGE_BYTES;
+                    const int k_el = kb * BK;
+                    mbar_arrive_expect_tx(fb, Cf::STAGE_BYTES);
+                    if (!p.a_mn) {
+                        tma_load_2d(sa, &tmA, fb, k_el, m0, policy);
+                    } else {
+#pragma unroll
+                        for (int c = 0; c < BM / 64; ++c)
+                            tma_load_2d(sa + c * MN_CHUNK_BYTES, &tmA, fb, m0 + 64 * c, k_el, policy);
+                    }
+                    if (!p.b_mn) {
+                        tma_load_2d(sb, &tmB, fb, k_el, n0, policy);
+                    } else {
+#pragma unroll
+                        for (int c = 0; c < BN / 64; ++c)
+                            tma_load_2d(sb + c * MN_CHUNK_BYTES, &tmB, fb, n0 + 64 * c, k_el, policy);
+                    }
+                    filled |= 1u << stage;
+                    fill_parity = (fill_parity & ~(1u << stage)) | (phase << stage);
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            // every copy this thread issued must land before the CTA exits
+            for (int s = 0; s < STAGES; ++s)
+                if (filled & (1u << s))
+                    mbar_wait(full_bar(s), (fill_parity >> s) & 1u, p.pipe_limit_ns);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            Cursor cur;
+            cursor_init(p.s, cta, cur);
+            Unit u;
+            int stage = 0;
+            uint32_t phase = 0, iter = 0;
+            bool ok = true;
+            while (ok && cursor_next(p.s, cta, cur, u)) {
+                const int buf = iter & 1;
+                if (!mbar_wait(tempty_bar(buf), ((iter >> 1) & 1u) ^ 1u, p.pipe_limit_ns)) {
+                    fail_pipe();
+                    break;
+                }
+                tc_fence_after_sync();
+                const uint32_t d_tmem = tmem_base + (uint32_t)(buf * BN);
+                for (int kb = u.k0; kb < u.k1; ++kb) {
+                    if (!mbar_wait(full_bar(stage), phase, p.pipe_limit_ns)) {
+                        fail_pipe();
+                        ok = false;
+                        break;
+                    }
+                    if (*abort_flag) { ok = false; break; }
+                    tc_fence_after_sync();
+                    const uint32_t sa = sbase + stage * Cf::STAGE_BYTES;
+                    const uint32_t sb = sa + A_STAGE_BYTES;
+#pragma unroll
+                    for (int kk = 0; kk < BK / UMMA_K; ++kk) {
+                        // K-major: a k-step of 16 elements is 32 bytes along the
+                        // swizzled row.  MN-major: 16 k-rows of 128 bytes.
+                        const uint64_t adesc =
+                            p.a_mn ? smem_desc_sw128(sa + kk * 16 * 128, MN_CHUNK_BYTES, SW_ATOM_BYTES)
+                                   : smem_desc_sw128(sa + kk * UMMA_K * 2, 16, SW_ATOM_BYTES);
+                        const uint64_t bdesc =
+                            p.b_mn ? smem_desc_sw128(sb + kk * 16 * 128, MN_CHUNK_BYTES, SW_ATOM_BYTES)
+                                   : smem_desc_sw128(sb + kk * UMMA_K * 2, 16, SW_ATOM_BYTES);
+                        mma_f16_ss(d_tmem, adesc, bdesc, p.idesc, (kb > u.k0 || kk > 0) ? 1u : 0u);
+                    }
+                    mma_commit(empty_bar(stage));
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                mma_commit(tfull_bar(buf));
+                ++iter;
+            }
+            // all MMAs this thread issued are complete before TMEM is freed
+            mma_commit(done_bar);
+            mbar_wait(done_bar, 0, p.pipe_limit_ns);
+        }
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const int q = warp & 3;              // TMEM lanes this warp may read: 32q .. 32q+31
+        const int row_in_tile = q * 32 + lane;
+        const int et = threadIdx.x - EPI_WARP0 * 32;
+        Cursor cur;
+        cursor_init(p.s, cta, cur);
+        Unit u;
+        uint32_t iter = 0;
+        while (cursor_next(p.s, cta, cur, u)) {
+            const int buf = iter & 1;
+            bool ok = mbar_wait(tfull_bar(buf), (iter >> 1) & 1u, p.pipe_limit_ns) && !*abort_flag;
+            if (!epi_vote_all(ok)) {
+                if (et == 0) fail_pipe();
+                break;
+            }
+            tc_fence_after_sync();
+            const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BN);
+            const int rows_valid = min(BM, p.M - u.tm * BM);
+            const int row = u.tm * BM + row_in_tile;
+            const bool row_ok = row_in_tile < rows_valid;
+
+            if (u.role == ROLE_PEER) {
+                // fp32 partial -> this CTA's slot, laid out [chunk][vec][row] so
+                // a warp's 16-byte stores cover 512 contiguous bytes
+                float4* slot = reinterpret_cast<float4*>(p.partials + (size_t)cta * BM * BN);
+#pragma unroll 1
+                for (int j = 0; j < BN / 32; ++j) {
+                    uint32_t r[32];
+                    __syncwarp();
+                    tmem_ld_32x32b_x32(tbase + j * 32, r);
+                    if (row_ok) {
+#pragma unroll
+                        for (int v = 0; v < 8; ++v)
+                            st_f4(slot + (size_t)(j * 8 + v) * BM + row_in_tile,
+                                  make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
+                                              __uint_as_float(r[4 * v + 2]),
+                                              __uint_as_float(r[4 * v + 3])));
+                    }
+                }
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(tempty_bar(buf));
+                __threadfence();
+                named_bar_sync(BAR_EPI_SYNC, EPI_THREADS);
+                if (et == 0 && cta != p.inject_skip_cta) post_flag(p.flags + u.tile, p.epoch);
+            } else {
+                bool store = true;
+                if (u.role == ROLE_OWNER) {
+                    const uint64_t target = ((uint64_t)p.epoch << 32) | (uint32_t)u.npeers;
+                    bool got = wait_flag(p.flags + u.tile, target, p.wait_limit_ns);
+                    store = epi_vote_all(got);
+                    if (!store && et == 0) record_status(p.status, STATUS_FLAG_TIMEOUT);
+                }
+                uint8_t* crow = reinterpret_cast<uint8_t*>(p.C) + ((size_t)row * p.N) * 2;
+#pragma unroll 1
+                for (int j = 0; j < BN / 32; ++j) {
+                    uint32_t r[32];
+                    __syncwarp();
+                    tmem_ld_32x32b_x32(tbase + j * 32, r);
+                    float acc[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) acc[i] = __uint_as_float(r[i]);
+                    if (u.role == ROLE_OWNER && store && row_ok) {
+                        // peers in ascending k: CTAs cta+1 .. cta+npeers
+#pragma unroll 1
+                        for (int pp = 1; pp <= u.npeers; ++pp) {
+                            const float4* slot = reinterpret_cast<const float4*>(
+                                p.partials + (size_t)(cta + pp) * BM * BN);
+#pragma unroll
+                            for (int v = 0; v < 8; ++v) {
+                                float4 x = ld_cg_f4(slot + (size_t)(j * 8 + v) * BM + row_in_tile);
+                                acc[4 * v] += x.x;
+                                acc[4 * v + 1] += x.y;
+                                acc[4 * v + 2] += x.z;
+                                acc[4 * v + 3] += x.w;
+                            }
+                        }
+                    }
+                    if (store && row_ok) {
+                        const int col0 = u.tn * BN + j * 32;
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) {
+                            const int col = col0 + 8 * v;
+                            if (col < p.N)
+                                st_u4(crow + (size_t)col * 2, pack2<OUT_BF16>(acc[8 * v], acc[8 * v + 1]),
+                                      pack2<OUT_BF16>(acc[8 * v + 2], acc[8 * v + 3]),
+                                      pack2<OUT_BF16>(acc[8 * v + 4], acc[8 * v + 5]),
+                                      pack2<OUT_BF16>(acc[8 * v + 6], acc[8 * v + 7]));
+                        }
+                    }
+                }
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(tempty_bar(buf));
+            }
+            ++iter;
+        }
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after_sync();
+        tmem_dealloc(tmem_base, Cf::TMEM_COLS);
+    }
+}
+
+}  // namespace psm

@@ -1,0 +1,182 @@
+"""CPU checks of the C-ABI library: it loads, exports every declared entry
+point, and its scheduler (the code the kernel runs, enumerated on the host)
+matches the oracle's restatement of the Stream-K decomposition unit by unit.
+No compute calls: there is no GPU here."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from oracle.streamk_schedule import Schedule
+from persistent_stream_matmul_gb300 import _binding as B
+from persistent_stream_matmul_gb300 import build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return B.load()
+
+
+def declared_functions():
+    names = []
+    for h in os.listdir(os.path.join(ROOT, "include")):
+        if h.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", h)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names += re.findall(r"\b(gemm_\w+)\s*\(", text)
+    return sorted(set(names))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert len(names) >= 12
+    raw = ctypes.CDLL(B.LIB_PATH)
+    for n in names:
+        assert hasattr(raw, n), n
+    assert sorted(B.SIGNATURES) == names
+
+
+def test_status_strings(lib):
+    for s in range(8):
+        assert B.gemm_status_string(s).startswith("GEMM_")
+    assert "UNKNOWN" in B.gemm_status_string(99)
+
+
+def _roles_from_oracle(o: Schedule):
+    contrib = o.contributors()
+    out = {}
+    for pid in range(o.g):
+        units = []
+        for tile, k0, k1 in o.segments(pid):
+            if k0 > 0:
+                units.append((tile, k0, k1, B.ROLE_PEER, 0))
+            elif k1 == o.ipt:
+                units.append((tile, k0, k1, B.ROLE_FULL, 0))
+            else:
+                units.append((tile, k0, k1, B.ROLE_OWNER, len(contrib[tile]) - 1))
+        out[pid] = units
+    return out
+
+
+SHAPES = [
+    # the five measured workloads, small ragged cases, degenerate ones
+    (512, 512, 512), (8192, 8192, 8192), (2304, 2304, 8192), (8192, 14336, 4096),
+    (64, 8192, 8192), (300, 264, 200), (1, 8, 8), (129, 136, 72), (1000, 40, 4096),
+]
+
+
+@pytest.mark.parametrize("M,N,K", SHAPES)
+@pytest.mark.parametrize("sms", [148, 152])
+@pytest.mark.parametrize("tile_n", [128, 256])
+def test_streamk_units_match_oracle(lib, M, N, K, sms, tile_n):
+    for g, two in ((sms, 1), (7, 1), (sms, 0), (2, 1)):
+        p = B.Plan(M, N, K, B.GEMM_BF16, 0, 1, "streamk", offline_sms=sms, tile_n=tile_n,
+                   grid=g, two_tiles=two)
+        o = Schedule(M, N, K, 128, tile_n, 64, g, two_tiles=bool(two), group_m=8)
+        assert p.info("tiles") == o.tiles and p.info("sk_tiles") == o.sk_tiles
+        assert p.info("sk_iters_per_cta") == o.iters_per_prog
+        assert p.info("sk_iters_rem") == o.iters_rem
+        assert p.info("grid") == g
+        sk_units = _roles_from_oracle(o)
+        whole = []
+        for c in range(g):
+            got = p.units(c)
+            n_sk = len(sk_units[c])
+            assert got[:n_sk] == sk_units[c], (c, got[:n_sk], sk_units[c])
+            rest = [u[0] for u in got[n_sk:]]
+            assert all(u[1:] == (0, o.ipt, B.ROLE_FULL, 0) for u in got[n_sk:])
+            assert rest == list(range(o.sk_tiles + c, o.tiles, g))
+            whole += rest
+        assert sorted(whole) == o.whole_tiles()
+        ws = p.workspace_size
+        if o.sk_tiles:
+            assert ws == -(-o.sk_tiles * 8 // 256) * 256 + g * 128 * tile_n * 4
+        else:
+            assert ws == 0
+        p.close()
+
+
+@pytest.mark.parametrize("M,N,K", SHAPES)
+def test_dp_and_persistent_units(lib, M, N, K):
+    o = Schedule(M, N, K, 128, 128, 64, 0)
+    p = B.Plan(M, N, K, B.GEMM_F16, 0, 0, "dp", offline_sms=148, tile_n=128)
+    assert p.info("grid") == o.tiles and p.workspace_size == 0
+    for c in range(0, o.tiles, max(1, o.tiles // 50)):
+        assert p.units(c) == [(c, 0, o.ipt, B.ROLE_FULL, 0)]
+    p.close()
+    p = B.Plan(M, N, K, B.GEMM_F16, 0, 0, "persistent", offline_sms=148, tile_n=128)
+    g = min(148, o.tiles)
+    assert p.info("grid") == g and p.workspace_size == 0
+    seen = []
+    for c in range(g):
+        u = p.units(c)
+        assert [x[0] for x in u] == list(range(c, o.tiles, g))
+        seen += [x[0] for x in u]
+    assert sorted(seen) == list(range(o.tiles))
+    p.close()
+
+
+@pytest.mark.parametrize("group_m", [0, 1, 3, 8])
+def test_raster_matches_oracle(lib, group_m):
+    for M, N in ((2304, 2304), (8192, 14336), (1000, 3000), (64, 8192)):
+        o = Schedule(M, N, 64, 128, 128, 64, 0, group_m=group_m)
+        p = B.Plan(M, N, 64, B.GEMM_F16, 0, 0, "persistent", offline_sms=148, tile_n=128,
+                   group_m=group_m)
+        for t in range(o.tiles):
+            assert p.tile_coords(t) == o.coords(t)
+        p.close()
+
+
+def test_default_options(lib):
+    p = B.Plan(8192, 8192, 8192, B.GEMM_BF16, 0, 1, "streamk", offline_sms=148)
+    assert p.info("tile_n") == 256 and p.info("group_m") == 8 and p.info("tile_k") == 64
+    assert p.info("tile_m") == 128
+    p.close()
+    p = B.Plan(64, 8192, 8192, B.GEMM_F16, 0, 0, "dp", offline_sms=148)
+    assert p.info("tile_n") == 128 and p.info("group_m") == 0 and p.info("tiles") == 64
+    p.close()
+
+
+def test_argument_errors(lib):
+    with pytest.raises(B.GemmError) as e:
+        B.gemm_plan_create_offline(-1, 8, 8, 0, 0, 0, 0, 148)
+    assert e.value.status == B.GEMM_ERR_INVALID_ARG
+    with pytest.raises(B.GemmError) as e:
+        B.gemm_plan_create_offline(8, 8, 8, 5, 0, 0, 0, 148)
+    assert e.value.status == B.GEMM_ERR_INVALID_ARG
+    with pytest.raises(B.GemmError) as e:
+        B.gemm_plan_create_offline(8, 8, 8, 0, 0, 0, 0, 0)
+    assert e.value.status == B.GEMM_ERR_INVALID_ARG
+    p = B.Plan(256, 256, 256, B.GEMM_F16, 0, 0, "streamk", offline_sms=148)
+    for key, val, st in ((B.GEMM_OPT_TILE_N, 64, B.GEMM_ERR_UNSUPPORTED),
+                         (B.GEMM_OPT_GRID, 149, B.GEMM_ERR_UNSUPPORTED),
+                         (B.GEMM_OPT_TWO_TILES, 2, B.GEMM_ERR_UNSUPPORTED),
+                         (99, 0, B.GEMM_ERR_INVALID_ARG)):
+        with pytest.raises(B.GemmError) as e:
+            p.set_option(key, val)
+        assert e.value.status == st
+    with pytest.raises(B.GemmError) as e:
+        p.units(148)
+    assert e.value.status == B.GEMM_ERR_INVALID_ARG
+    with pytest.raises(B.GemmError) as e:
+        p.run(16, 16, 16, 16)
+    assert e.value.status == B.GEMM_ERR_NO_DEVICE
+    assert B.gemm_last_status(p.handle) == B.GEMM_ERR_NO_DEVICE
+    assert lib.gemm_plan_destroy(None) == 0
+    p.close()
+
+
+def test_owner_peer_structure_on_workloads(lib):
+    # among a CTA's Stream-K units, only the first may be a PEER and only the last an OWNER
+    for M, N, K in SHAPES:
+        p = B.Plan(M, N, K, B.GEMM_BF16, 0, 1, "streamk", offline_sms=148, tile_n=128)
+        sk = p.info("sk_tiles")
+        for c in range(p.info("grid")):
+            roles = [u[3] for u in p.units(c) if u[0] < sk]
+            assert B.ROLE_PEER not in roles[1:]
+            assert B.ROLE_OWNER not in roles[:-1]
+        p.close()

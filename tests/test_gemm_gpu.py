@@ -1,0 +1,195 @@
+"""GPU parity: the CUDA library (through its C ABI) against the CPU oracle.
+
+Bar: every element within |C - C_ref| <= 2^-8 |C_ref| + K 2^-22 sum|a||b|;
+bit-exact on integer-valued inputs; bitwise identical from run to run."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from persistent_stream_matmul_gb300 import _binding as B
+from persistent_stream_matmul_gb300 import inputs
+from tests.gpu_util import Workspace, ensure_built, run, to_device
+
+pytestmark = pytest.mark.gpu
+
+SCHEDS = ["dp", "persistent", "streamk"]
+LAYOUTS = [(0, 0), (0, 1), (1, 0), (1, 1)]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    ensure_built()
+    oracle.build()
+
+
+def _case(M, N, K, dtype, la, lb, law, seed):
+    A, Bm = inputs.operands(M, N, K, dtype, la, lb, law, law, seed)
+    return A, Bm, to_device(A), to_device(Bm)
+
+
+def _check_full(Cb, A, Bm, M, N, K, dtype, la, lb, exact=False):
+    C64, S, Cref = oracle.gemm(A, Bm, M, N, K, dtype, la, lb)
+    if exact:
+        assert np.array_equal(Cb, Cref), "integer inputs must be bit-exact"
+    ok, worst, nbad = oracle.check(Cb, dtype, C64, S, K)
+    assert ok, "%d elements outside the bound (worst ratio %.3g)" % (nbad, worst)
+    return Cref
+
+
+# ------------------------------------------------------------------ small shapes
+SMALL = [(300, 264, 200), (129, 136, 72), (257, 520, 1000), (1, 8, 8), (64, 512, 4096),
+         (128, 256, 64), (640, 384, 520)]
+
+
+@pytest.mark.parametrize("sched", SCHEDS)
+@pytest.mark.parametrize("dtype", [inputs.F16, inputs.BF16])
+@pytest.mark.parametrize("la,lb", LAYOUTS)
+def test_parity_small(sched, dtype, la, lb):
+    ws = Workspace()
+    for i, (M, N, K) in enumerate(SMALL):
+        if la == 1 and M % 8:
+            continue
+        A, Bm, dA, dB = _case(M, N, K, dtype, la, lb, ("normal", 1.0), 10 + i)
+        for tile_n in (128, 256):
+            p = B.Plan(M, N, K, dtype, la, lb, sched, tile_n=tile_n)
+            Cb = run(p, dA, dB, M, N, ws)
+            _check_full(Cb, A, Bm, M, N, K, dtype, la, lb)
+            p.close()
+
+
+@pytest.mark.parametrize("sched", SCHEDS)
+@pytest.mark.parametrize("dtype", [inputs.F16, inputs.BF16])
+@pytest.mark.parametrize("la,lb", LAYOUTS)
+def test_integer_bit_exact_small(sched, dtype, la, lb):
+    ws = Workspace()
+    for i, (M, N, K) in enumerate(SMALL):
+        if la == 1 and M % 8:
+            continue
+        A, Bm, dA, dB = _case(M, N, K, dtype, la, lb, inputs.INT_LAW, 50 + i)
+        p = B.Plan(M, N, K, dtype, la, lb, sched)
+        Cb = run(p, dA, dB, M, N, ws)
+        _check_full(Cb, A, Bm, M, N, K, dtype, la, lb, exact=True)
+        p.close()
+
+
+@pytest.mark.parametrize("dtype", [inputs.F16, inputs.BF16])
+def test_streamk_forced_grids_integer(dtype):
+    # several contributors per tile; every grid must give the oracle's bits
+    M, N, K = 384, 512, 2048
+    A, Bm, dA, dB = _case(M, N, K, dtype, 0, 0, inputs.INT_LAW, 7)
+    _, _, Cref = oracle.gemm(A, Bm, M, N, K, dtype, 0, 0)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    ws = Workspace()
+    for tile_n in (128, 256):
+        tiles = 3 * (N // tile_n)
+        for g in sorted({1, 2, 7, tiles, sms}):
+            for two in (0, 1):
+                p = B.Plan(M, N, K, dtype, 0, 0, "streamk", tile_n=tile_n, grid=g, two_tiles=two)
+                Cb = run(p, dA, dB, M, N, ws)
+                assert np.array_equal(Cb, Cref), (tile_n, g, two)
+                p.close()
+
+
+def test_streamk_deterministic_and_within_bound():
+    M, N, K, dtype = 512, 768, 3000 // 8 * 8, inputs.BF16
+    A, Bm, dA, dB = _case(M, N, K, dtype, 0, 1, ("normal", 1.0), 8)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    ws = Workspace()
+    for g in (5, sms):
+        p = B.Plan(M, N, K, dtype, 0, 1, "streamk", tile_n=128, grid=g)
+        first = run(p, dA, dB, M, N, ws)
+        _check_full(first, A, Bm, M, N, K, dtype, 0, 1)
+        for _ in range(10):
+            assert np.array_equal(run(p, dA, dB, M, N, ws), first)
+        p.close()
+
+
+def test_schedules_agree_on_integers():
+    M, N, K, dtype = 520, 1000, 1032, inputs.F16
+    A, Bm, dA, dB = _case(M, N, K, dtype, 0, 0, inputs.INT_LAW, 9)
+    outs = []
+    for s in SCHEDS:
+        p = B.Plan(M, N, K, dtype, 0, 0, s)
+        outs.append(run(p, dA, dB, M, N))
+        p.close()
+    assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[0], outs[2])
+
+
+# ------------------------------------------------------------------ edge cases
+def test_k_zero_gives_zero_and_empty_is_noop():
+    p = B.Plan(100, 64, 0, inputs.F16, 0, 0, "streamk")
+    dA = torch.zeros(8, dtype=torch.int16, device="cuda")
+    Cb = run(p, dA, dA, 100, 64)
+    assert not Cb.any()
+    p.close()
+    for M, N in ((0, 64), (64, 0)):
+        p = B.Plan(M, N, 64, inputs.F16, 0, 0, "streamk")
+        p.run(0, 0, 0, None)
+        assert p.last_status() == B.GEMM_OK
+        p.close()
+
+
+def test_unsupported_alignment_and_strides():
+    p = B.Plan(64, 64, 64, inputs.F16, 0, 0, "dp")
+    buf = torch.zeros(64 * 64 + 8, dtype=torch.int16, device="cuda")
+    with pytest.raises(B.GemmError) as e:
+        p.run(buf.data_ptr() + 2, buf, buf)
+    assert e.value.status == B.GEMM_ERR_UNSUPPORTED
+    p.close()
+    p = B.Plan(64, 64, 60, inputs.F16, 0, 0, "dp")
+    with pytest.raises(B.GemmError) as e:
+        p.run(buf, buf, buf)
+    assert e.value.status == B.GEMM_ERR_UNSUPPORTED
+    p.close()
+    p = B.Plan(64, 512, 512, inputs.F16, 0, 0, "streamk")
+    assert p.workspace_size > 0
+    with pytest.raises(B.GemmError) as e:
+        p.run(buf, buf, buf, None)
+    assert e.value.status == B.GEMM_ERR_WORKSPACE
+    p.close()
+
+
+def test_timeout_is_reported_and_gpu_stays_healthy():
+    # a peer that never posts: its owner's bounded wait must run out, the
+    # tile's C must stay untouched, and the next run must be correct
+    M, N, K, dtype = 128, 128, 4096, inputs.F16
+    A, Bm, dA, dB = _case(M, N, K, dtype, 0, 0, inputs.INT_LAW, 11)
+    p = B.Plan(M, N, K, dtype, 0, 0, "streamk", tile_n=128, grid=4, wait_limit_us=2000)
+    units = [p.units(c) for c in range(4)]
+    assert units[0][0][3] == B.ROLE_OWNER and units[1][0][3] == B.ROLE_PEER
+    p.set_option(B.GEMM_OPT_INJECT_SKIP_POST, 1)
+    ws = Workspace()
+    with pytest.raises(B.GemmError) as e:
+        run(p, dA, dB, M, N, ws)
+    assert e.value.status == B.GEMM_ERR_TIMEOUT
+    # C untouched: run again by hand and look at the sentinel
+    from tests.gpu_util import GUARD, SENTINEL
+    Cbuf = torch.full((M * N + 2 * GUARD,), SENTINEL - 65536, dtype=torch.int16, device="cuda")
+    p.run(dA, dB, Cbuf.data_ptr() + 2 * GUARD, ws.get(p.workspace_size))
+    assert p.last_status() == B.GEMM_ERR_TIMEOUT
+    assert (Cbuf.cpu().numpy().view(np.uint16) == SENTINEL).all()
+    assert p.last_status() == B.GEMM_OK  # cleared by the previous read
+    p.set_option(B.GEMM_OPT_INJECT_SKIP_POST, -1)
+    Cb = run(p, dA, dB, M, N, ws)
+    _check_full(Cb, A, Bm, M, N, K, dtype, 0, 0, exact=True)
+    p.close()
+
+
+def test_run_host_end_to_end():
+    M, N, K, dtype = 256, 384, 640, inputs.BF16
+    A, Bm = inputs.operands(M, N, K, dtype, 0, 1, ("normal", 1.0), ("normal", 1.0), 12)
+    hA = torch.from_numpy(A.view(np.int16)).pin_memory()
+    hB = torch.from_numpy(Bm.view(np.int16)).pin_memory()
+    hC = torch.empty(M * N, dtype=torch.int16).pin_memory()
+    dA = torch.empty_like(hA, device="cuda")
+    dB = torch.empty_like(hB, device="cuda")
+    dC = torch.empty(M * N, dtype=torch.int16, device="cuda")
+    p = B.Plan(M, N, K, dtype, 0, 1, "streamk")
+    ws = Workspace()
+    stream = torch.cuda.current_stream()
+    p.run_host(hA, hB, hC, dA, dB, dC, ws.get(p.workspace_size), stream)
+    assert p.last_status(stream) == B.GEMM_OK
+    Cb = hC.numpy().view(np.uint16).reshape(M, N)
+    _check_full(Cb, A, Bm, M, N, K, dtype, 0, 1)
+    p.close()
