@@ -37,7 +37,7 @@ def run(plan: B.Plan, dA: torch.Tensor, dB: torch.Tensor, M: int, N: int, ws: Wo
         stream=None, check_guard=True):
     """C = A*B on the GPU; returns C as uint16 (M, N) numpy, guards verified."""
     ws = ws or Workspace()
-    Cbuf = torch.full((M * N + 2 * GUARD,), SENTINEL - 65536, dtype=torch.int16, device="cuda")
+    Cbuf = torch.full((M * N + 2 * GUARD,), SENTINEL, dtype=torch.int16, device="cuda")
     cptr = Cbuf.data_ptr() + 2 * GUARD
     w = ws.get(plan.workspace_size)
     plan.run(dA, dB, cptr, w, stream)

@@ -165,7 +165,7 @@ def test_timeout_is_reported_and_gpu_stays_healthy():
     assert e.value.status == B.GEMM_ERR_TIMEOUT
     # C untouched: run again by hand and look at the sentinel
     from tests.gpu_util import GUARD, SENTINEL
-    Cbuf = torch.full((M * N + 2 * GUARD,), SENTINEL - 65536, dtype=torch.int16, device="cuda")
+    Cbuf = torch.full((M * N + 2 * GUARD,), SENTINEL, dtype=torch.int16, device="cuda")
     p.run(dA, dB, Cbuf.data_ptr() + 2 * GUARD, ws.get(p.workspace_size))
     assert p.last_status() == B.GEMM_ERR_TIMEOUT
     assert (Cbuf.cpu().numpy().view(np.uint16) == SENTINEL).all()
