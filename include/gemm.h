@@ -174,6 +174,32 @@ gemm_status_t gemm_run_host(gemm_plan_t plan, const void *hA, const void *hB, vo
                             void *dA, void *dB, void *dC, void *workspace,
                             gemm_stream_t stream);
 
+/* Size of the fixed scratch array behind gemm_run_no_alloc: 16 MiB. */
+#define GEMM_NO_ALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
+
+/*
+ * Same product as gemm_run, for callers that cannot allocate device memory
+ * (for example a plug-in inside a framework that owns all device memory and
+ * forbids allocation on its execution path).  The pages have no counterpart:
+ * this is a library convenience.  The caller passes A, B and C as for
+ * gemm_run but no workspace: the Stream-K flags and partial tiles go to a
+ * fixed 16 MiB device array inside the library, which each GPU that loads the
+ * library holds until the process exits.  Nothing is allocated by this call
+ * (no cudaMalloc, cudaFree or allocating library routine).
+ *  - Plans whose gemm_workspace_size exceeds GEMM_NO_ALLOC_SCRATCH_BYTES are
+ *    rejected with GEMM_ERR_WORKSPACE (choose GEMM_OPT_TILE_N = 128 or a
+ *    smaller GEMM_OPT_GRID to fit).  Plans that need no workspace just run.
+ *  - The first call on a device looks up the array's device address (with
+ *    that device current); make that first call before any stream capture.
+ *  - Every call shares the one array and finds the last call's data in it;
+ *    each call clears the flag part on `stream` before its kernel.  Calls
+ *    that overlap on the GPU (other streams, other threads) race: serialise
+ *    them.
+ * Errors: as gemm_run, plus WORKSPACE as above.
+ */
+gemm_status_t gemm_run_no_alloc(gemm_plan_t plan, const void *A, const void *B, void *C,
+                                gemm_stream_t stream);
+
 /*
  * Synchronise `stream`, then read and clear the plan's device status word.
  * Returns GEMM_OK, GEMM_ERR_TIMEOUT (a bounded device wait expired since the

@@ -48,6 +48,7 @@ SIGNATURES = {
     "gemm_run": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp]),
     "gemm_run_host": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
     "gemm_last_status": (_i32, [_vp, _vp]),
+    "gemm_run_no_alloc": (_i32, [_vp, _vp, _vp, _vp, _vp]),
     "gemm_plan_units": (_i32, [_vp, _i64, ctypes.POINTER(ctypes.c_int32), _i64,
                                ctypes.POINTER(_i64)]),
     "gemm_plan_tile_coords": (_i32, [_vp, _i64, ctypes.POINTER(_i64), ctypes.POINTER(_i64)]),
@@ -145,6 +146,16 @@ def gemm_run(plan, A, B, C, workspace=None, stream=None):
 def gemm_run_host(plan, hA, hB, hC, dA, dB, dC, workspace=None, stream=None):
     _check(load().gemm_run_host(plan, _addr(hA), _addr(hB), _addr(hC), _addr(dA), _addr(dB),
                                 _addr(dC), _addr(workspace), _stream(stream)), "gemm_run_host")
+
+
+def gemm_run_no_alloc(plan, A, B, C, stream=None):
+    """gemm_run without a workspace argument: the library's fixed scratch array
+    is used instead, so nothing is allocated (for callers that cannot allocate)."""
+    _check(load().gemm_run_no_alloc(plan, _addr(A), _addr(B), _addr(C), _stream(stream)),
+           "gemm_run_no_alloc")
+
+
+GEMM_NO_ALLOC_SCRATCH_BYTES = 16 * 1024 * 1024
 
 
 def gemm_last_status(plan, stream=None) -> int:

@@ -539,3 +539,58 @@ const char* gemm_status_string(gemm_status_t s) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Allocation-free entry point.
+//
+// Some callers cannot call cudaMalloc: for example a plug-in that runs inside
+// a host framework which owns every byte of device memory and forbids
+// allocation on its execution path, or a caller whose memory budget is fixed
+// before the first product runs.  gemm_run_no_alloc serves them: instead of a
+// caller-provided workspace, the Stream-K flags and partial tiles live in the
+// fixed array below, which every GPU that loads this library holds until the
+// process exits.  Plans whose workspace exceeds it are rejected.
+//
+// The array's name is a host-side stand-in in host code, not a device
+// address, so the host looks up the real address once per device with
+// cudaGetSymbolAddress, with that device current, on the first call for that
+// device.  Every call shares the array and finds the previous call's data in
+// it; calls that overlap on the GPU race on it.
+static __device__ __align__(256) unsigned char psm_no_alloc_scratch[GEMM_NO_ALLOC_SCRATCH_BYTES];
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_no_alloc_mu;
+void* g_no_alloc_ptr[kMaxDevices];
+}  // namespace
+
+extern "C" gemm_status_t gemm_run_no_alloc(gemm_plan_t p, const void* A, const void* B, void* C,
+                                           gemm_stream_t stream) {
+    if (!p) return GEMM_ERR_INVALID_ARG;
+    if (p->offline) return GEMM_ERR_NO_DEVICE;
+    if (p->ws_bytes > (size_t)GEMM_NO_ALLOC_SCRATCH_BYTES) return GEMM_ERR_WORKSPACE;
+    if (p->ws_bytes == 0) return gemm_run(p, A, B, C, nullptr, stream);
+    if (p->device < 0 || p->device >= kMaxDevices) return GEMM_ERR_UNSUPPORTED;
+    void* scratch = nullptr;
+    {
+        DeviceGuard guard(p->device);  // the look-up must run with the plan's device current
+        if (!guard.ok) return GEMM_ERR_CUDA;
+        std::lock_guard<std::mutex> lock(g_no_alloc_mu);
+        if (!g_no_alloc_ptr[p->device]) {
+            void* ptr = nullptr;
+            if (cudaGetSymbolAddress(&ptr, psm_no_alloc_scratch) != cudaSuccess || !ptr) {
+                cudaGetLastError();
+                return GEMM_ERR_CUDA;
+            }
+            g_no_alloc_ptr[p->device] = ptr;
+        }
+        scratch = g_no_alloc_ptr[p->device];
+        // the flags left by an earlier call (possibly of another plan) are cleared
+        // so this run starts from zero; the partial slots are always written
+        // before they are read
+        if (cudaMemsetAsync(scratch, 0, p->ws_flag_bytes, reinterpret_cast<cudaStream_t>(stream)) !=
+            cudaSuccess)
+            return GEMM_ERR_CUDA;
+    }
+    return gemm_run(p, A, B, C, scratch, stream);
+}
