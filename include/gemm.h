@@ -94,12 +94,19 @@ enum {
     GEMM_OPT_WAIT_LIMIT_US = 5,
     /* test hook: the CTA with this index skips posting its peer flag, so its
      * owner's wait runs out.  -1 (default) = off. */
-    GEMM_OPT_INJECT_SKIP_POST = 6
+    GEMM_OPT_INJECT_SKIP_POST = 6,
+    /* CTAs per cluster along M: 1, or 2 (two CTAs on adjacent 128-row halves
+     * of a 256-row tile share one B tile, each loading half and multicasting
+     * it to both).  0 (default) lets the plan choose (2 for wide tiles with at
+     * least two row tiles).  With 2, the scheduler's tiles are 256 rows tall,
+     * GEMM_OPT_GRID counts CTAs (pairs of them form one scheduling unit). */
+    GEMM_OPT_CLUSTER_M = 7
 };
 
 /* Keys for gemm_plan_get_info. */
 enum {
-    GEMM_INFO_TILE_M = 1, GEMM_INFO_TILE_N = 2, GEMM_INFO_TILE_K = 3,
+    GEMM_INFO_TILE_M = 1,           /* rows of a scheduled tile: 128 x cluster size */
+    GEMM_INFO_TILE_N = 2, GEMM_INFO_TILE_K = 3,
     GEMM_INFO_TILES_M = 4, GEMM_INFO_TILES_N = 5, GEMM_INFO_TILES = 6,
     GEMM_INFO_ITERS_PER_TILE = 7,   /* k-iterations per tile, ceil(K / 64) */
     GEMM_INFO_GRID = 8,             /* CTAs launched by gemm_run */
@@ -109,7 +116,8 @@ enum {
     GEMM_INFO_NUM_SMS = 12,
     GEMM_INFO_STAGES = 13,          /* depth of the shared-memory ring */
     GEMM_INFO_GROUP_M = 14,
-    GEMM_INFO_SMEM_BYTES = 15       /* dynamic shared memory per CTA */
+    GEMM_INFO_SMEM_BYTES = 15,      /* dynamic shared memory per CTA */
+    GEMM_INFO_CLUSTER_M = 16        /* CTAs per cluster (1 or 2) */
 };
 
 /* Roles of a work unit reported by gemm_plan_units. */
@@ -209,7 +217,9 @@ gemm_status_t gemm_last_status(gemm_plan_t plan, gemm_stream_t stream);
 
 /*
  * Host twin of the device tile scheduler: the work units CTA `cta` executes,
- * in order, 5 int32 per unit: tile id (raster order), first k-iteration,
+ * in order (the two CTAs of a cluster execute the same units, each on its
+ * 128-row half of the GEMM_INFO_TILE_M-row tile), 5 int32 per unit: tile id
+ * (raster order), first k-iteration,
  * end k-iteration, role (GEMM_ROLE_*), peers (for an OWNER: how many peer
  * partials it adds; else 0).  Writes at most max_units units to `units`
  * (may be NULL when max_units is 0) and the full count to *n_units.

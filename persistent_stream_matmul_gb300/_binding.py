@@ -28,11 +28,12 @@ GEMM_OPT_TILE_N = 3
 GEMM_OPT_TWO_TILES = 4
 GEMM_OPT_WAIT_LIMIT_US = 5
 GEMM_OPT_INJECT_SKIP_POST = 6
+GEMM_OPT_CLUSTER_M = 7
 
 INFO = {
     "tile_m": 1, "tile_n": 2, "tile_k": 3, "tiles_m": 4, "tiles_n": 5, "tiles": 6,
     "iters_per_tile": 7, "grid": 8, "sk_tiles": 9, "sk_iters_per_cta": 10,
-    "sk_iters_rem": 11, "num_sms": 12, "stages": 13, "group_m": 14, "smem_bytes": 15,
+    "sk_iters_rem": 11, "num_sms": 12, "stages": 13, "group_m": 14, "smem_bytes": 15, "cluster_m": 16,
 }
 ROLE_FULL, ROLE_OWNER, ROLE_PEER = 0, 1, 2
 
@@ -199,7 +200,7 @@ class Plan:
                                                    offline_sms)
         keys = {"grid": GEMM_OPT_GRID, "group_m": GEMM_OPT_GROUP_M, "tile_n": GEMM_OPT_TILE_N,
                 "two_tiles": GEMM_OPT_TWO_TILES, "wait_limit_us": GEMM_OPT_WAIT_LIMIT_US,
-                "inject_skip_post": GEMM_OPT_INJECT_SKIP_POST}
+                "inject_skip_post": GEMM_OPT_INJECT_SKIP_POST, "cluster_m": GEMM_OPT_CLUSTER_M}
         for k, v in options.items():
             if v is not None:
                 gemm_plan_set_option(self.handle, keys[k], int(v))

@@ -56,10 +56,11 @@ struct gemm_plan {
     int dtype, layout_a, layout_b, schedule;
     int device, num_sms, offline;
     // options
-    int opt_grid, opt_group_m, opt_tile_n, opt_two_tiles, inject_skip;
+    int opt_grid, opt_group_m, opt_tile_n, opt_two_tiles, inject_skip, opt_cluster_m;
     int64_t wait_limit_us;
+    int max_pair_ctas;  // CTAs co-resident as 2-CTA clusters (0: unknown)
     // derived
-    int BN, stages, smem_bytes;
+    int BN, CM, ctas, stages, smem_bytes;
     Sched s;
     size_t ws_flag_bytes, ws_bytes;
     // device state
@@ -70,7 +71,7 @@ struct gemm_plan {
     bool tm_valid;
     CUtensorMap tmA, tmB;
     const void* flags_cleared_for;
-    bool attr_set[2];
+    bool attr_set[8];
 };
 
 namespace {
@@ -80,14 +81,24 @@ bool valid_enums(int dtype, int la, int lb, int sched) {
            (lb == 0 || lb == 1) && (sched >= 0 && sched <= 2);
 }
 
-template <int BN, bool BF>
+template <int BN, bool BF, int CM>
 void* kernel_ptr() {
-    return reinterpret_cast<void*>(&gemm_kernel<BN, BF>);
+    return reinterpret_cast<void*>(&gemm_kernel<BN, BF, CM>);
 }
 
-void* pick_kernel(int BN, int dtype) {
-    if (BN == 256) return dtype == GEMM_BF16 ? kernel_ptr<256, true>() : kernel_ptr<256, false>();
-    return dtype == GEMM_BF16 ? kernel_ptr<128, true>() : kernel_ptr<128, false>();
+template <int CM>
+void* pick_kernel_cm(int BN, int dtype) {
+    if (BN == 256)
+        return dtype == GEMM_BF16 ? kernel_ptr<256, true, CM>() : kernel_ptr<256, false, CM>();
+    return dtype == GEMM_BF16 ? kernel_ptr<128, true, CM>() : kernel_ptr<128, false, CM>();
+}
+
+void* pick_kernel(int BN, int dtype, int CM) {
+    return CM == 2 ? pick_kernel_cm<2>(BN, dtype) : pick_kernel_cm<1>(BN, dtype);
+}
+
+int kernel_index(int BN, int dtype, int CM) {
+    return (BN == 256 ? 4 : 0) + (dtype == GEMM_BF16 ? 2 : 0) + (CM == 2 ? 1 : 0);
 }
 
 int smem_for(int BN) { return BN == 256 ? Cfg<256>::SMEM_BYTES : Cfg<128>::SMEM_BYTES; }
@@ -98,12 +109,18 @@ int stages_for(int BN) { return BN == 256 ? Cfg<256>::STAGES : Cfg<128>::STAGES;
 // wrapper: tile counts, Stream-K tile count with the two_tiles rule, even
 // split of the Stream-K iterations).
 gemm_status_t derive(gemm_plan* p) {
-    const int64_t tiles_m = cdiv64(p->M, BM);
+    const int64_t tiles_m128 = cdiv64(p->M, BM);
     int BN = p->opt_tile_n;
     if (BN == 0) {
-        const int64_t tiles256 = tiles_m * cdiv64(p->N, 256);
+        const int64_t tiles256 = tiles_m128 * cdiv64(p->N, 256);
         BN = (p->N > 128 && tiles256 >= p->num_sms) ? 256 : 128;
     }
+    // 2-CTA clusters share B between two 128-row halves: worth it when there
+    // are at least two row tiles and the tile is wide (compute-bound shapes)
+    int CM = p->opt_cluster_m;
+    if (CM == 0) CM = (tiles_m128 >= 2 && BN == 256) ? 2 : 1;
+    // the scheduler works on tiles of CM*128 rows and on units of CM CTAs
+    const int64_t tiles_m = cdiv64(p->M, (int64_t)BM * CM);
     const int64_t tiles_n = cdiv64(p->N, BN);
     const int64_t tiles = tiles_m * tiles_n;
     const int64_t ipt = cdiv64(p->K, BK);
@@ -116,7 +133,9 @@ gemm_status_t derive(gemm_plan* p) {
     s.ipt = (int32_t)(ipt > 0 ? ipt : 1);
     s.group_m = p->opt_group_m >= 0 ? p->opt_group_m
                                     : (p->schedule == GEMM_SCHED_DATA_PARALLEL ? 0 : 8);
-    const int g = p->opt_grid > 0 ? p->opt_grid : p->num_sms;
+    int g_ctas = p->opt_grid > 0 ? p->opt_grid : p->num_sms;
+    if (CM == 2 && p->max_pair_ctas > 0 && g_ctas > p->max_pair_ctas) g_ctas = p->max_pair_ctas;
+    const int g = g_ctas / CM > 0 ? g_ctas / CM : 1;  // scheduling units
     s.sk_tiles = 0;
     s.sk_q = s.sk_r = 0;
     if (p->schedule == GEMM_SCHED_DATA_PARALLEL) {
@@ -137,17 +156,53 @@ gemm_status_t derive(gemm_plan* p) {
     }
     p->s = s;
     p->BN = BN;
+    p->CM = CM;
+    p->ctas = s.grid * CM;
     p->stages = stages_for(BN);
     p->smem_bytes = smem_for(BN);
     if (p->schedule == GEMM_SCHED_STREAMK && s.sk_tiles > 0) {
-        p->ws_flag_bytes = ((size_t)s.sk_tiles * 8 + 255) / 256 * 256;
-        p->ws_bytes = p->ws_flag_bytes + (size_t)s.grid * BM * BN * sizeof(float);
+        p->ws_flag_bytes = ((size_t)s.sk_tiles * CM * 8 + 255) / 256 * 256;
+        p->ws_bytes = p->ws_flag_bytes + (size_t)p->ctas * BM * BN * sizeof(float);
     } else {
         p->ws_flag_bytes = 0;
         p->ws_bytes = 0;
     }
     p->tm_valid = false;
     return GEMM_OK;
+}
+
+// CTAs that can be resident at once as 2-CTA clusters of the (largest) kernel
+// configuration; clusters live inside one GPC, so this can be below #SMs.
+int max_pair_ctas(int dev) {
+    static std::mutex mu;
+    static int cache[64];
+    std::lock_guard<std::mutex> lock(mu);
+    if (dev < 0 || dev >= 64) return 0;
+    if (cache[dev]) return cache[dev];
+    void* fn = pick_kernel(256, GEMM_BF16, 2);
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_for(256)) !=
+        cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(2, 1, 1);
+    cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = (size_t)smem_for(256);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, fn, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    cache[dev] = 2 * n;
+    return cache[dev];
 }
 
 gemm_status_t make_plan(gemm_plan_t* out, int64_t M, int64_t N, int64_t K, int dtype, int la,
@@ -169,6 +224,7 @@ gemm_status_t make_plan(gemm_plan_t* out, int64_t M, int64_t N, int64_t K, int d
     p->opt_tile_n = 0;
     p->opt_two_tiles = 1;
     p->inject_skip = -1;
+    p->opt_cluster_m = 0;
     p->wait_limit_us = 1000000;
     if (offline) {
         if (num_sms <= 0) { delete p; return GEMM_ERR_INVALID_ARG; }
@@ -192,6 +248,7 @@ gemm_status_t make_plan(gemm_plan_t* out, int64_t M, int64_t N, int64_t K, int d
         if (major != 10 || minor != 3) { delete p; return GEMM_ERR_NO_DEVICE; }
         p->device = dev;
         p->num_sms = sms;
+        p->max_pair_ctas = max_pair_ctas(dev);
         if (cudaMalloc(&p->d_status, sizeof(int)) != cudaSuccess ||
             cudaMemset(p->d_status, 0, sizeof(int)) != cudaSuccess) {
             if (p->d_status) cudaFree(p->d_status);
@@ -207,13 +264,13 @@ gemm_status_t make_plan(gemm_plan_t* out, int64_t M, int64_t N, int64_t K, int d
     }
     if (getenv("GEMM_DEBUG")) {
         fprintf(stderr,
-                "[gemm] M=%lld N=%lld K=%lld dtype=%d A=%s B=%s sched=%d | tile 128x%dx64 "
-                "tiles %dx%d=%d ipt=%d grid=%d sk_tiles=%d sk_q=%lld sk_r=%lld group_m=%d "
-                "ws=%zu smem=%d\n",
+                "[gemm] M=%lld N=%lld K=%lld dtype=%d A=%s B=%s sched=%d | tile %dx%dx64 "
+                "(cluster %d) tiles %dx%d=%d ipt=%d units=%d ctas=%d sk_tiles=%d sk_q=%lld "
+                "sk_r=%lld group_m=%d ws=%zu smem=%d pair_ctas=%d\n",
                 (long long)M, (long long)N, (long long)K, dtype, la ? "col" : "row",
-                lb ? "col" : "row", sched, p->BN, p->s.tiles_m, p->s.tiles_n, p->s.tiles,
-                p->s.ipt, p->s.grid, p->s.sk_tiles, (long long)p->s.sk_q, (long long)p->s.sk_r,
-                p->s.group_m, p->ws_bytes, p->smem_bytes);
+                lb ? "col" : "row", sched, BM * p->CM, p->BN, p->CM, p->s.tiles_m, p->s.tiles_n,
+                p->s.tiles, p->s.ipt, p->s.grid, p->ctas, p->s.sk_tiles, (long long)p->s.sk_q,
+                (long long)p->s.sk_r, p->s.group_m, p->ws_bytes, p->smem_bytes, p->max_pair_ctas);
     }
     *out = p;
     return GEMM_OK;
@@ -252,7 +309,7 @@ gemm_status_t encode_maps(gemm_plan* p, const void* A, const void* B) {
         if (p->layout_b == GEMM_COL_MAJOR) {
             dims[0] = (cuuint64_t)p->K; dims[1] = (cuuint64_t)p->N;
             strides[0] = (cuuint64_t)p->K * 2;
-            box[0] = BK; box[1] = (cuuint32_t)p->BN;
+            box[0] = BK; box[1] = (cuuint32_t)(p->BN / p->CM);  // each CTA of a pair loads half
         } else {
             dims[0] = (cuuint64_t)p->N; dims[1] = (cuuint64_t)p->K;
             strides[0] = (cuuint64_t)p->N * 2;
@@ -328,6 +385,10 @@ gemm_status_t gemm_plan_set_option(gemm_plan_t p, int key, int64_t value) {
             if (value < -1 || value > 65535) return GEMM_ERR_UNSUPPORTED;
             p->inject_skip = (int)value;
             return GEMM_OK;
+        case GEMM_OPT_CLUSTER_M:
+            if (value != 0 && value != 1 && value != 2) return GEMM_ERR_UNSUPPORTED;
+            p->opt_cluster_m = (int)value;
+            break;
         default:
             return GEMM_ERR_INVALID_ARG;
     }
@@ -340,14 +401,14 @@ gemm_status_t gemm_plan_get_info(gemm_plan_t p, int key, int64_t* value) {
     if (!p || !value) return GEMM_ERR_INVALID_ARG;
     int64_t v;
     switch (key) {
-        case GEMM_INFO_TILE_M: v = BM; break;
+        case GEMM_INFO_TILE_M: v = (int64_t)BM * p->CM; break;
         case GEMM_INFO_TILE_N: v = p->BN; break;
         case GEMM_INFO_TILE_K: v = BK; break;
         case GEMM_INFO_TILES_M: v = p->s.tiles_m; break;
         case GEMM_INFO_TILES_N: v = p->s.tiles_n; break;
         case GEMM_INFO_TILES: v = p->s.tiles; break;
         case GEMM_INFO_ITERS_PER_TILE: v = cdiv64(p->K, BK); break;
-        case GEMM_INFO_GRID: v = p->s.grid; break;
+        case GEMM_INFO_GRID: v = p->ctas; break;
         case GEMM_INFO_SK_TILES: v = p->s.sk_tiles; break;
         case GEMM_INFO_SK_ITERS_PER_CTA: v = p->s.sk_q; break;
         case GEMM_INFO_SK_ITERS_REM: v = p->s.sk_r; break;
@@ -355,6 +416,7 @@ gemm_status_t gemm_plan_get_info(gemm_plan_t p, int key, int64_t* value) {
         case GEMM_INFO_STAGES: v = p->stages; break;
         case GEMM_INFO_GROUP_M: v = p->s.group_m; break;
         case GEMM_INFO_SMEM_BYTES: v = p->smem_bytes; break;
+        case GEMM_INFO_CLUSTER_M: v = p->CM; break;
         default: return GEMM_ERR_INVALID_ARG;
     }
     *value = v;
@@ -390,8 +452,8 @@ gemm_status_t gemm_run(gemm_plan_t p, const void* A, const void* B, void* C, voi
     gemm_status_t es = encode_maps(p, A, B);
     if (es != GEMM_OK) return es;
 
-    void* fn = pick_kernel(p->BN, p->dtype);
-    const int bi = p->BN == 256 ? 1 : 0;
+    void* fn = pick_kernel(p->BN, p->dtype, p->CM);
+    const int bi = kernel_index(p->BN, p->dtype, p->CM);
     if (!p->attr_set[bi]) {
         if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, p->smem_bytes) !=
             cudaSuccess)
@@ -424,19 +486,37 @@ gemm_status_t gemm_run(gemm_plan_t p, const void* A, const void* B, void* C, voi
     kp.pipe_limit_ns = 4000000000ull;
 
     cudaLaunchConfig_t cfg{};
-    cfg.gridDim = dim3((unsigned)p->s.grid, 1, 1);
+    cfg.gridDim = dim3((unsigned)p->ctas, 1, 1);
     cfg.blockDim = dim3(NUM_THREADS, 1, 1);
     cfg.dynamicSmemBytes = (size_t)p->smem_bytes;
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeCooperative;
-    attr[0].val.cooperative = 1;
-    if (p->schedule == GEMM_SCHED_STREAMK) {
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
+    cudaLaunchAttribute attr[2];
+    unsigned na = 0;
+    if (p->CM == 2) {
+        attr[na].id = cudaLaunchAttributeClusterDimension;
+        attr[na].val.clusterDim.x = 2;
+        attr[na].val.clusterDim.y = 1;
+        attr[na].val.clusterDim.z = 1;
+        ++na;
     }
+    // Stream-K CTAs wait on one another: ask for co-residency
+    const bool coop = p->schedule == GEMM_SCHED_STREAMK;
+    if (coop) {
+        attr[na].id = cudaLaunchAttributeCooperative;
+        attr[na].val.cooperative = 1;
+        ++na;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = na;
     void* args[3] = {&p->tmA, &p->tmB, &kp};
     cudaError_t e = cudaLaunchKernelExC(&cfg, fn, args);
+    if (e != cudaSuccess && coop && p->CM == 2) {
+        // cooperative + cluster refused: the grid is already sized to the
+        // co-resident cluster count, so launch without the attribute
+        cudaGetLastError();
+        cfg.numAttrs = na - 1;
+        e = cudaLaunchKernelExC(&cfg, fn, args);
+    }
     if (e != cudaSuccess) {
         cudaGetLastError();
         return GEMM_ERR_LAUNCH;
@@ -486,14 +566,15 @@ gemm_status_t gemm_last_status(gemm_plan_t p, gemm_stream_t stream) {
 
 gemm_status_t gemm_plan_units(gemm_plan_t p, int64_t cta, int32_t* units, int64_t max_units,
                               int64_t* n_units) {
-    if (!p || !n_units || cta < 0 || cta >= p->s.grid || max_units < 0 ||
+    if (!p || !n_units || cta < 0 || cta >= p->ctas || max_units < 0 ||
         (max_units > 0 && !units))
         return GEMM_ERR_INVALID_ARG;
+    const int32_t unit_cta = (int32_t)(cta / p->CM);  // both CTAs of a pair run the same units
     Cursor cur;
-    cursor_init(p->s, (int32_t)cta, cur);
+    cursor_init(p->s, unit_cta, cur);
     Unit u;
     int64_t n = 0;
-    while (cursor_next(p->s, (int32_t)cta, cur, u)) {
+    while (cursor_next(p->s, unit_cta, cur, u)) {
         if (n < max_units) {
             int32_t* o = units + 5 * n;
             o[0] = u.tile;

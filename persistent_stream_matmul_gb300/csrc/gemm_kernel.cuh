@@ -3,6 +3,13 @@
 // Stream-K schedules; the tile scheduler (sched.cuh) tells every CTA which
 // work units (tile, k-range, role) it runs.
 //
+// Clusters (CM = 2): the two CTAs of a cluster run the same scheduled unit on
+// the two 128-row halves of a 256-row tile, so they need the same B tile.
+// Each CTA loads its own A and half of B, multicasting that half into both
+// CTAs' rings; a stage's empty barrier counts the MMA commits of both CTAs, so
+// neither refills a stage the other is still reading.  L2-to-SM traffic per
+// CTA drops from A + B to A + B/2 per k-slice.
+//
 // Warp roles (192 threads, one CTA per SM):
 //   warp 0      TMA producer: one lane fills a STAGES-deep ring of A/B tiles
 //               in shared memory (128-byte swizzle), guarded by full/empty
@@ -135,12 +142,14 @@ __device__ __forceinline__ uint32_t pack2(float a, float b) {
     }
 }
 
-template <int BN, bool OUT_BF16>
+template <int BN, bool OUT_BF16, int CM>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ KParams p) {
     using Cf = Cfg<BN>;
     constexpr int STAGES = Cf::STAGES;
+    static_assert(CM == 1 || CM == 2, "cluster size");
+    constexpr uint16_t PAIR = 0x3;
     extern __shared__ uint8_t smem_raw[];
 
     // 1024-byte aligned base: the 128-byte swizzle pattern repeats every 1 KB
@@ -159,12 +168,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int cta = blockIdx.x;
+    const int cta = blockIdx.x;                      // workspace slot of this CTA
+    const int unit_cta = blockIdx.x / CM;            // index the scheduler knows
+    const int rank = CM == 2 ? (int)cluster_ctarank() : 0;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(full_bar(s), 1);
-            mbar_init(empty_bar(s), 1);
+            mbar_init(empty_bar(s), CM);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(tfull_bar(b), 1);
@@ -183,7 +194,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         tmem_relinquish();
     }
     tc_fence_before_sync();
-    __syncthreads();
+    if constexpr (CM == 2) {
+        cluster_sync_all();  // the peer's barriers exist before anything is multicast
+    } else {
+        __syncthreads();
+    }
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
 
@@ -197,14 +212,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (lane == 0) {
             const uint64_t policy = l2_policy_evict_normal();
             Cursor cur;
-            cursor_init(p.s, cta, cur);
+            cursor_init(p.s, unit_cta, cur);
             Unit u;
             int stage = 0;
             uint32_t phase = 0;
             uint32_t filled = 0, fill_parity = 0;  // per-stage bit masks
             bool ok = true;
-            while (ok && cursor_next(p.s, cta, cur, u)) {
-                const int m0 = u.tm * BM, n0 = u.tn * BN;
+            while (ok && cursor_next(p.s, unit_cta, cur, u)) {
+                const int m0 = (u.tm * CM + rank) * BM, n0 = u.tn * BN;
                 for (int kb = u.k0; kb < u.k1; ++kb) {
                     if (!mbar_wait(empty_bar(stage), phase ^ 1u, p.pipe_limit_ns)) {
                         fail_pipe();
@@ -224,12 +239,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         for (int c = 0; c < BM / 64; ++c)
                             tma_load_2d(sa + c * MN_CHUNK_BYTES, &tmA, fb, m0 + 64 * c, k_el, policy);
                     }
-                    if (!p.b_mn) {
-                        tma_load_2d(sb, &tmB, fb, k_el, n0, policy);
-                    } else {
+                    if constexpr (CM == 1) {
+                        if (!p.b_mn) {
+                            tma_load_2d(sb, &tmB, fb, k_el, n0, policy);
+                        } else {
 #pragma unroll
-                        for (int c = 0; c < BN / 64; ++c)
-                            tma_load_2d(sb + c * MN_CHUNK_BYTES, &tmB, fb, n0 + 64 * c, k_el, policy);
+                            for (int c = 0; c < BN / 64; ++c)
+                                tma_load_2d(sb + c * MN_CHUNK_BYTES, &tmB, fb, n0 + 64 * c, k_el,
+                                            policy);
+                        }
+                    } else {
+                        // this CTA's half of B, into both CTAs of the pair
+                        if (!p.b_mn) {
+                            const int half = BN / 2;  // rows of the K-major box
+                            tma_load_2d_multicast(sb + rank * half * 128, &tmB, fb, k_el,
+                                                  n0 + rank * half, PAIR, policy);
+                        } else {
+#pragma unroll
+                            for (int c = rank * (BN / 128); c < (rank + 1) * (BN / 128); ++c)
+                                tma_load_2d_multicast(sb + c * MN_CHUNK_BYTES, &tmB, fb,
+                                                      n0 + 64 * c, k_el, PAIR, policy);
+                        }
                     }
                     filled |= 1u << stage;
                     fill_parity = (fill_parity & ~(1u << stage)) | (phase << stage);
@@ -239,21 +269,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     }
                 }
             }
-            // every copy this thread issued must land before the CTA exits
+            // before the CTA (or its peer) exits: every copy into this CTA has
+            // landed, and every MMA that reads this CTA's ring (the peer's too)
+            // has released it
             for (int s = 0; s < STAGES; ++s)
-                if (filled & (1u << s))
+                if (filled & (1u << s)) {
                     mbar_wait(full_bar(s), (fill_parity >> s) & 1u, p.pipe_limit_ns);
+                    mbar_wait(empty_bar(s), (fill_parity >> s) & 1u, p.pipe_limit_ns);
+                }
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             Cursor cur;
-            cursor_init(p.s, cta, cur);
+            cursor_init(p.s, unit_cta, cur);
             Unit u;
             int stage = 0;
             uint32_t phase = 0, iter = 0;
             bool ok = true;
-            while (ok && cursor_next(p.s, cta, cur, u)) {
+            while (ok && cursor_next(p.s, unit_cta, cur, u)) {
                 const int buf = iter & 1;
                 if (!mbar_wait(tempty_bar(buf), ((iter >> 1) & 1u) ^ 1u, p.pipe_limit_ns)) {
                     fail_pipe();
@@ -283,7 +317,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                    : smem_desc_sw128(sb + kk * UMMA_K * 2, 16, SW_ATOM_BYTES);
                         mma_f16_ss(d_tmem, adesc, bdesc, p.idesc, (kb > u.k0 || kk > 0) ? 1u : 0u);
                     }
-                    mma_commit(empty_bar(stage));
+                    if constexpr (CM == 2) {
+                        mma_commit_multicast(empty_bar(stage), PAIR);  // both halves of B were read
+                    } else {
+                        mma_commit(empty_bar(stage));
+                    }
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1u;
@@ -303,10 +341,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int row_in_tile = q * 32 + lane;
         const int et = threadIdx.x - EPI_WARP0 * 32;
         Cursor cur;
-        cursor_init(p.s, cta, cur);
+        cursor_init(p.s, unit_cta, cur);
         Unit u;
         uint32_t iter = 0;
-        while (cursor_next(p.s, cta, cur, u)) {
+        while (cursor_next(p.s, unit_cta, cur, u)) {
             const int buf = iter & 1;
             bool ok = mbar_wait(tfull_bar(buf), (iter >> 1) & 1u, p.pipe_limit_ns) && !*abort_flag;
             if (!epi_vote_all(ok)) {
@@ -315,8 +353,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
             tc_fence_after_sync();
             const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BN);
-            const int rows_valid = min(BM, p.M - u.tm * BM);
-            const int row = u.tm * BM + row_in_tile;
+            const int tm = u.tm * CM + rank;  // this CTA's 128-row tile
+            const int rows_valid = min(BM, p.M - tm * BM);
+            const int row = tm * BM + row_in_tile;
             const bool row_ok = row_in_tile < rows_valid;
 
             if (u.role == ROLE_PEER) {
@@ -342,12 +381,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 if (lane == 0) mbar_arrive(tempty_bar(buf));
                 __threadfence();
                 named_bar_sync(BAR_EPI_SYNC, EPI_THREADS);
-                if (et == 0 && cta != p.inject_skip_cta) post_flag(p.flags + u.tile, p.epoch);
+                if (et == 0 && cta != p.inject_skip_cta) post_flag(p.flags + u.tile * CM + rank, p.epoch);
             } else {
                 bool store = true;
                 if (u.role == ROLE_OWNER) {
                     const uint64_t target = ((uint64_t)p.epoch << 32) | (uint32_t)u.npeers;
-                    bool got = wait_flag(p.flags + u.tile, target, p.wait_limit_ns);
+                    bool got = wait_flag(p.flags + u.tile * CM + rank, target, p.wait_limit_ns);
                     store = epi_vote_all(got);
                     if (!store && et == 0) record_status(p.status, STATUS_FLAG_TIMEOUT);
                 }
@@ -361,11 +400,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
                     for (int i = 0; i < 32; ++i) acc[i] = __uint_as_float(r[i]);
                     if (u.role == ROLE_OWNER && store && row_ok) {
-                        // peers in ascending k: CTAs cta+1 .. cta+npeers
+                        // peers in ascending k: the same half of units unit_cta+1 ..
 #pragma unroll 1
                         for (int pp = 1; pp <= u.npeers; ++pp) {
                             const float4* slot = reinterpret_cast<const float4*>(
-                                p.partials + (size_t)(cta + pp) * BM * BN);
+                                p.partials + (size_t)((unit_cta + pp) * CM + rank) * BM * BN);
 #pragma unroll
                             for (int v = 0; v < 8; ++v) {
                                 float4 x = ld_cg_f4(slot + (size_t)(j * 8 + v) * BM + row_in_tile);
@@ -398,7 +437,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
 
     tc_fence_before_sync();
-    __syncthreads();
+    __syncwarp();
+    if constexpr (CM == 2) {
+        cluster_sync_all();  // neither CTA leaves while the other may still signal it
+    } else {
+        __syncthreads();
+    }
     if (warp == 1) {
         __syncwarp();
         tc_fence_after_sync();

@@ -72,29 +72,34 @@ SHAPES = [
 @pytest.mark.parametrize("M,N,K", SHAPES)
 @pytest.mark.parametrize("sms", [148, 152])
 @pytest.mark.parametrize("tile_n", [128, 256])
-def test_streamk_units_match_oracle(lib, M, N, K, sms, tile_n):
-    for g, two in ((sms, 1), (7, 1), (sms, 0), (2, 1)):
+@pytest.mark.parametrize("cm", [1, 2])
+def test_streamk_units_match_oracle(lib, M, N, K, sms, tile_n, cm):
+    for g, two in ((sms, 1), (8, 1), (sms, 0), (2, 1)):
         p = B.Plan(M, N, K, B.GEMM_BF16, 0, 1, "streamk", offline_sms=sms, tile_n=tile_n,
-                   grid=g, two_tiles=two)
-        o = Schedule(M, N, K, 128, tile_n, 64, g, two_tiles=bool(two), group_m=8)
+                   grid=g, two_tiles=two, cluster_m=cm)
+        gu = g // cm                       # scheduling units: pairs of CTAs when cm == 2
+        o = Schedule(M, N, K, 128 * cm, tile_n, 64, gu, two_tiles=bool(two), group_m=8)
+        assert p.info("cluster_m") == cm and p.info("tile_m") == 128 * cm
         assert p.info("tiles") == o.tiles and p.info("sk_tiles") == o.sk_tiles
         assert p.info("sk_iters_per_cta") == o.iters_per_prog
         assert p.info("sk_iters_rem") == o.iters_rem
-        assert p.info("grid") == g
+        assert p.info("grid") == gu * cm
         sk_units = _roles_from_oracle(o)
         whole = []
-        for c in range(g):
+        for c in range(gu * cm):
             got = p.units(c)
-            n_sk = len(sk_units[c])
-            assert got[:n_sk] == sk_units[c], (c, got[:n_sk], sk_units[c])
-            rest = [u[0] for u in got[n_sk:]]
-            assert all(u[1:] == (0, o.ipt, B.ROLE_FULL, 0) for u in got[n_sk:])
-            assert rest == list(range(o.sk_tiles + c, o.tiles, g))
-            whole += rest
+            u = c // cm
+            n_sk = len(sk_units[u])
+            assert got[:n_sk] == sk_units[u], (c, got[:n_sk], sk_units[u])
+            rest = [x[0] for x in got[n_sk:]]
+            assert all(x[1:] == (0, o.ipt, B.ROLE_FULL, 0) for x in got[n_sk:])
+            assert rest == list(range(o.sk_tiles + u, o.tiles, gu))
+            if c % cm == 0:
+                whole += rest
         assert sorted(whole) == o.whole_tiles()
         ws = p.workspace_size
         if o.sk_tiles:
-            assert ws == -(-o.sk_tiles * 8 // 256) * 256 + g * 128 * tile_n * 4
+            assert ws == -(-o.sk_tiles * cm * 8 // 256) * 256 + gu * cm * 128 * tile_n * 4
         else:
             assert ws == 0
         p.close()
@@ -103,12 +108,13 @@ def test_streamk_units_match_oracle(lib, M, N, K, sms, tile_n):
 @pytest.mark.parametrize("M,N,K", SHAPES)
 def test_dp_and_persistent_units(lib, M, N, K):
     o = Schedule(M, N, K, 128, 128, 64, 0)
-    p = B.Plan(M, N, K, B.GEMM_F16, 0, 0, "dp", offline_sms=148, tile_n=128)
+    p = B.Plan(M, N, K, B.GEMM_F16, 0, 0, "dp", offline_sms=148, tile_n=128, cluster_m=1)
     assert p.info("grid") == o.tiles and p.workspace_size == 0
     for c in range(0, o.tiles, max(1, o.tiles // 50)):
         assert p.units(c) == [(c, 0, o.ipt, B.ROLE_FULL, 0)]
     p.close()
-    p = B.Plan(M, N, K, B.GEMM_F16, 0, 0, "persistent", offline_sms=148, tile_n=128)
+    p = B.Plan(M, N, K, B.GEMM_F16, 0, 0, "persistent", offline_sms=148, tile_n=128,
+               cluster_m=1)
     g = min(148, o.tiles)
     assert p.info("grid") == g and p.workspace_size == 0
     seen = []
@@ -134,7 +140,10 @@ def test_raster_matches_oracle(lib, group_m):
 def test_default_options(lib):
     p = B.Plan(8192, 8192, 8192, B.GEMM_BF16, 0, 1, "streamk", offline_sms=148)
     assert p.info("tile_n") == 256 and p.info("group_m") == 8 and p.info("tile_k") == 64
-    assert p.info("tile_m") == 128
+    assert p.info("cluster_m") == 2 and p.info("tile_m") == 256 and p.info("grid") == 148
+    p.close()
+    p = B.Plan(8192, 8192, 8192, B.GEMM_BF16, 0, 1, "streamk", offline_sms=148, cluster_m=1)
+    assert p.info("tile_m") == 128 and p.info("grid") == 148
     p.close()
     p = B.Plan(64, 8192, 8192, B.GEMM_F16, 0, 0, "dp", offline_sms=148)
     assert p.info("tile_n") == 128 and p.info("group_m") == 0 and p.info("tiles") == 64
@@ -173,7 +182,7 @@ def test_argument_errors(lib):
 def test_owner_peer_structure_on_workloads(lib):
     # among a CTA's Stream-K units, only the first may be a PEER and only the last an OWNER
     for M, N, K in SHAPES:
-        p = B.Plan(M, N, K, B.GEMM_BF16, 0, 1, "streamk", offline_sms=148, tile_n=128)
+        p = B.Plan(M, N, K, B.GEMM_BF16, 0, 1, "streamk", offline_sms=148)
         sk = p.info("sk_tiles")
         for c in range(p.info("grid")):
             roles = [u[3] for u in p.units(c) if u[0] < sk]

@@ -52,10 +52,11 @@ def test_parity_small(sched, dtype, la, lb):
             continue
         A, Bm, dA, dB = _case(M, N, K, dtype, la, lb, ("normal", 1.0), 10 + i)
         for tile_n in (128, 256):
-            p = B.Plan(M, N, K, dtype, la, lb, sched, tile_n=tile_n)
-            Cb = run(p, dA, dB, M, N, ws)
-            _check_full(Cb, A, Bm, M, N, K, dtype, la, lb)
-            p.close()
+            for cm in (1, 2):
+                p = B.Plan(M, N, K, dtype, la, lb, sched, tile_n=tile_n, cluster_m=cm)
+                Cb = run(p, dA, dB, M, N, ws)
+                _check_full(Cb, A, Bm, M, N, K, dtype, la, lb)
+                p.close()
 
 
 @pytest.mark.parametrize("sched", SCHEDS)
@@ -67,10 +68,11 @@ def test_integer_bit_exact_small(sched, dtype, la, lb):
         if la == 1 and M % 8:
             continue
         A, Bm, dA, dB = _case(M, N, K, dtype, la, lb, inputs.INT_LAW, 50 + i)
-        p = B.Plan(M, N, K, dtype, la, lb, sched)
-        Cb = run(p, dA, dB, M, N, ws)
-        _check_full(Cb, A, Bm, M, N, K, dtype, la, lb, exact=True)
-        p.close()
+        for cm in (1, 2):
+            p = B.Plan(M, N, K, dtype, la, lb, sched, cluster_m=cm)
+            Cb = run(p, dA, dB, M, N, ws)
+            _check_full(Cb, A, Bm, M, N, K, dtype, la, lb, exact=True)
+            p.close()
 
 
 @pytest.mark.parametrize("dtype", [inputs.F16, inputs.BF16])
@@ -82,13 +84,15 @@ def test_streamk_forced_grids_integer(dtype):
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     ws = Workspace()
     for tile_n in (128, 256):
-        tiles = 3 * (N // tile_n)
-        for g in sorted({1, 2, 7, tiles, sms}):
-            for two in (0, 1):
-                p = B.Plan(M, N, K, dtype, 0, 0, "streamk", tile_n=tile_n, grid=g, two_tiles=two)
-                Cb = run(p, dA, dB, M, N, ws)
-                assert np.array_equal(Cb, Cref), (tile_n, g, two)
-                p.close()
+        for cm in (1, 2):
+            tiles = -(-3 // cm) * (N // tile_n)
+            for g in sorted({2, 8, 14, tiles * cm, sms}):
+                for two in (0, 1):
+                    p = B.Plan(M, N, K, dtype, 0, 0, "streamk", tile_n=tile_n, grid=g,
+                               two_tiles=two, cluster_m=cm)
+                    Cb = run(p, dA, dB, M, N, ws)
+                    assert np.array_equal(Cb, Cref), (tile_n, cm, g, two)
+                    p.close()
 
 
 def test_streamk_deterministic_and_within_bound():
@@ -110,10 +114,12 @@ def test_schedules_agree_on_integers():
     A, Bm, dA, dB = _case(M, N, K, dtype, 0, 0, inputs.INT_LAW, 9)
     outs = []
     for s in SCHEDS:
-        p = B.Plan(M, N, K, dtype, 0, 0, s)
-        outs.append(run(p, dA, dB, M, N))
-        p.close()
-    assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[0], outs[2])
+        for cm in (1, 2):
+            p = B.Plan(M, N, K, dtype, 0, 0, s, cluster_m=cm)
+            outs.append(run(p, dA, dB, M, N))
+            p.close()
+    for o in outs[1:]:
+        assert np.array_equal(outs[0], o)
 
 
 # ------------------------------------------------------------------ edge cases
@@ -173,6 +179,29 @@ def test_timeout_is_reported_and_gpu_stays_healthy():
     p.set_option(B.GEMM_OPT_INJECT_SKIP_POST, -1)
     Cb = run(p, dA, dB, M, N, ws)
     _check_full(Cb, A, Bm, M, N, K, dtype, 0, 0, exact=True)
+    p.close()
+
+
+def test_timeout_with_clusters_hits_only_the_silent_half():
+    # pairs of CTAs: the peer CTA 2 (unit 1, lower half) stays silent, so only
+    # the lower half's owner (CTA 0) gives up; the upper half completes
+    M, N, K, dtype = 256, 128, 4096, inputs.F16
+    A, Bm, dA, dB = _case(M, N, K, dtype, 0, 0, inputs.INT_LAW, 13)
+    _, _, Cref = oracle.gemm(A, Bm, M, N, K, dtype, 0, 0)
+    p = B.Plan(M, N, K, dtype, 0, 0, "streamk", tile_n=128, grid=8, cluster_m=2,
+               wait_limit_us=2000, inject_skip_post=2)
+    assert p.info("tile_m") == 256 and p.info("grid") == 8
+    assert p.units(0)[0][3] == B.ROLE_OWNER and p.units(2)[0][3] == B.ROLE_PEER
+    from tests.gpu_util import GUARD, SENTINEL
+    ws = Workspace()
+    Cbuf = torch.full((M * N + 2 * GUARD,), SENTINEL, dtype=torch.int16, device="cuda")
+    p.run(dA, dB, Cbuf.data_ptr() + 2 * GUARD, ws.get(p.workspace_size))
+    assert p.last_status() == B.GEMM_ERR_TIMEOUT
+    host = Cbuf.cpu().numpy().view(np.uint16)[GUARD:GUARD + M * N].reshape(M, N)
+    assert (host[:128] == SENTINEL).all()
+    assert np.array_equal(host[128:], Cref[128:])
+    p.set_option(B.GEMM_OPT_INJECT_SKIP_POST, -1)
+    assert np.array_equal(run(p, dA, dB, M, N, ws), Cref)
     p.close()
 
 
