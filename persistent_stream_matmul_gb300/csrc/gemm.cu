@@ -499,9 +499,13 @@ gemm_status_t gemm_run(gemm_plan_t p, const void* A, const void* B, void* C, voi
         attr[na].val.clusterDim.z = 1;
         ++na;
     }
-    // Stream-K CTAs wait on one another: ask for co-residency
-    const bool coop = p->schedule == GEMM_SCHED_STREAMK;
-    if (coop) {
+    // Stream-K CTAs wait on one another, so all must be resident at once.
+    // Without clusters a cooperative launch guarantees it.  Cluster launches
+    // are never made cooperative: their grid is sized to the number of
+    // clusters that fit at once (cudaOccupancyMaxActiveClusters), and the
+    // owners' waits are bounded, so a peer that is not resident turns into
+    // GEMM_ERR_TIMEOUT rather than a hang.
+    if (p->schedule == GEMM_SCHED_STREAMK && p->CM == 1) {
         attr[na].id = cudaLaunchAttributeCooperative;
         attr[na].val.cooperative = 1;
         ++na;
@@ -510,13 +514,6 @@ gemm_status_t gemm_run(gemm_plan_t p, const void* A, const void* B, void* C, voi
     cfg.numAttrs = na;
     void* args[3] = {&p->tmA, &p->tmB, &kp};
     cudaError_t e = cudaLaunchKernelExC(&cfg, fn, args);
-    if (e != cudaSuccess && coop && p->CM == 2) {
-        // cooperative + cluster refused: the grid is already sized to the
-        // co-resident cluster count, so launch without the attribute
-        cudaGetLastError();
-        cfg.numAttrs = na - 1;
-        e = cudaLaunchKernelExC(&cfg, fn, args);
-    }
     if (e != cudaSuccess) {
         cudaGetLastError();
         return GEMM_ERR_LAUNCH;

@@ -210,7 +210,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (warp == 0) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
-            const uint64_t policy = l2_policy_evict_normal();
+            // With a single row of tiles every B tile is read exactly once:
+            // let it leave L2 first and keep the small, shared A resident.
+            const bool b_once = p.s.tiles_m == 1;
+            const uint64_t pol_a = b_once ? l2_policy_evict_last() : l2_policy_evict_normal();
+            const uint64_t policy = b_once ? l2_policy_evict_first() : l2_policy_evict_normal();
             Cursor cur;
             cursor_init(p.s, unit_cta, cur);
             Unit u;
@@ -233,11 +237,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     const int k_el = kb * BK;
                     mbar_arrive_expect_tx(fb, Cf::STAGE_BYTES);
                     if (!p.a_mn) {
-                        tma_load_2d(sa, &tmA, fb, k_el, m0, policy);
+                        tma_load_2d(sa, &tmA, fb, k_el, m0, pol_a);
                     } else {
 #pragma unroll
                         for (int c = 0; c < BM / 64; ++c)
-                            tma_load_2d(sa + c * MN_CHUNK_BYTES, &tmA, fb, m0 + 64 * c, k_el, policy);
+                            tma_load_2d(sa + c * MN_CHUNK_BYTES, &tmA, fb, m0 + 64 * c, k_el, pol_a);
                     }
                     if constexpr (CM == 1) {
                         if (!p.b_mn) {
@@ -401,17 +405,36 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     for (int i = 0; i < 32; ++i) acc[i] = __uint_as_float(r[i]);
                     if (u.role == ROLE_OWNER && store && row_ok) {
                         // peers in ascending k: the same half of units unit_cta+1 ..
+                        // Loads of PEER_BATCH peers are issued before any of them is
+                        // added, so 32 16-byte loads per thread are in flight; the
+                        // additions keep the ascending order.
+                        constexpr int PEER_BATCH = 4;
+                        const float4* base = reinterpret_cast<const float4*>(p.partials) +
+                                             (size_t)(j * 8) * BM + row_in_tile;
+                        const size_t slot_f4 = (size_t)BM * BN / 4;
 #pragma unroll 1
-                        for (int pp = 1; pp <= u.npeers; ++pp) {
-                            const float4* slot = reinterpret_cast<const float4*>(
-                                p.partials + (size_t)((unit_cta + pp) * CM + rank) * BM * BN);
+                        for (int pp = 1; pp <= u.npeers; pp += PEER_BATCH) {
+                            float4 x[PEER_BATCH][8];
 #pragma unroll
-                            for (int v = 0; v < 8; ++v) {
-                                float4 x = ld_cg_f4(slot + (size_t)(j * 8 + v) * BM + row_in_tile);
-                                acc[4 * v] += x.x;
-                                acc[4 * v + 1] += x.y;
-                                acc[4 * v + 2] += x.z;
-                                acc[4 * v + 3] += x.w;
+                            for (int q = 0; q < PEER_BATCH; ++q) {
+                                if (pp + q <= u.npeers) {
+                                    const float4* slot =
+                                        base + (size_t)((unit_cta + pp + q) * CM + rank) * slot_f4;
+#pragma unroll
+                                    for (int v = 0; v < 8; ++v) x[q][v] = ld_cg_f4(slot + (size_t)v * BM);
+                                }
+                            }
+#pragma unroll
+                            for (int q = 0; q < PEER_BATCH; ++q) {
+                                if (pp + q <= u.npeers) {
+#pragma unroll
+                                    for (int v = 0; v < 8; ++v) {
+                                        acc[4 * v] += x[q][v].x;
+                                        acc[4 * v + 1] += x[q][v].y;
+                                        acc[4 * v + 2] += x[q][v].z;
+                                        acc[4 * v + 3] += x[q][v].w;
+                                    }
+                                }
                             }
                         }
                     }
