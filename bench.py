@@ -203,6 +203,33 @@ def config_of(spec, schedule, n):
                 2 * (spec["M"] * spec["K"] + spec["K"] * spec["N"]) / 1e6)}
 
 
+# --------------------------------------------------------------------- ranks
+def max_over_ranks(value: float, dist, world: int, device) -> float:
+    """Max of a per-rank number over all ranks (the slowest rank sets the time)."""
+    if world <= 1:
+        return float(value)
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(flops_per_step: float, steps: int, world: int, max_ms: float) -> float:
+    """Aggregate throughput: every rank ran `steps` steps; time = slowest rank."""
+    return world * steps * flops_per_step / (max_ms * 1e-3) / 1e12
+
+
+def sm_busy_fraction(stamps: np.ndarray, num_sms: int) -> dict:
+    """From per-CTA (start, ready, loads_done, end) stamps: the share of SM time
+    occupied by CTAs between the first start and the last end, and the span."""
+    start, end = stamps[:, 0].astype(np.float64), stamps[:, 3].astype(np.float64)
+    span = end.max() - start.min()
+    busy = float(np.sum(end - start) / (num_sms * span)) if span > 0 else 0.0
+    last = np.sort(end)
+    return {"sm_busy_frac": busy, "span_us": span / 1e3,
+            "tail_us": float((last[-1] - np.median(last)) / 1e3)}
+
+
 # --------------------------------------------------------------------- GPU arm
 def main():
     ap = argparse.ArgumentParser()
@@ -285,6 +312,17 @@ def main():
         med = statistics.median(ms)
         per_sched[s] = {"tflops": flops / (med * 1e-3) / 1e12, "ms_median": med,
                         "ms_min": min(ms), "ms_max": max(ms)}
+        # one more (untimed) launch with per-CTA stamps: SM idle time at the tail
+        ctas = p.info("grid")
+        tbuf = torch.zeros(4 * ctas, dtype=torch.int64, device="cuda")
+        p.set_trace(tbuf, tbuf.numel() * 8)
+        p.run(dA, dB, dC, w, stream)
+        torch.cuda.synchronize()
+        p.set_trace(None, 0)
+        per_sched[s].update(sm_busy_fraction(tbuf.cpu().numpy().reshape(ctas, 4),
+                                             p.info("num_sms")))
+        per_sched[s]["ctas"] = ctas
+        per_sched[s]["tile"] = "%dx%dx64" % (p.info("tile_m"), p.info("tile_n"))
 
     best = max(per_sched, key=lambda s: per_sched[s]["tflops"])
     sched = best if args.schedule == "best" else args.schedule
@@ -305,11 +343,8 @@ def main():
     elapsed_ms = e0.elapsed_time(e1)
     if p.last_status(stream) != B.GEMM_OK:
         raise RuntimeError("device status after the timed region is not OK")
-    t = torch.tensor([elapsed_ms], dtype=torch.float64, device="cuda")
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    elapsed_ms = float(t.item())
-    value = world * args.steps * flops / (elapsed_ms * 1e-3) / 1e12
+    elapsed_ms = max_over_ranks(elapsed_ms, dist, world, "cuda")
+    value = whole_job_tflops(flops, args.steps, world, elapsed_ms)
     launch_ms = elapsed_ms / args.steps
 
     # end to end through the C ABI with host buffers: H2D A, B; GEMM; D2H C
@@ -330,10 +365,8 @@ def main():
         e3.record(stream)
         torch.cuda.synchronize()
         barrier()
-        te = torch.tensor([e2.elapsed_time(e3)], dtype=torch.float64, device="cuda")
-        if world > 1:
-            dist.all_reduce(te, op=dist.ReduceOp.MAX)
-        e2e = {"value": world * n_e2e * flops / (float(te.item()) * 1e-3) / 1e12,
+        te = max_over_ranks(e2.elapsed_time(e3), dist, world, "cuda")
+        e2e = {"value": whole_job_tflops(flops, n_e2e, world, te),
                "unit": "TFLOP/s", "steps": n_e2e,
                "h2d_bytes_per_step": int(hA.numel() * 2 + hB.numel() * 2),
                "d2h_bytes_per_step": int(hC.numel() * 2)}

@@ -34,7 +34,9 @@
  *    Otherwise gemm_run returns GEMM_ERR_UNSUPPORTED.
  *  - gemm_run is asynchronous on the given stream.  Launch errors return at
  *    once; a device-side wait that ran out of time is reported by
- *    gemm_last_status.
+ *    gemm_last_status.  Kernels are launched as programmatic dependents: a
+ *    launch may begin while the previous kernel in the stream finishes, but
+ *    it reads and writes global memory only after that kernel has completed.
  *  - A plan is not thread-safe.  Two runs that share one workspace must not
  *    overlap in time (use one stream or order them).
  */
@@ -228,6 +230,17 @@ gemm_status_t gemm_last_status(gemm_plan_t plan, gemm_stream_t stream);
  */
 gemm_status_t gemm_plan_units(gemm_plan_t plan, int64_t cta, int32_t *units,
                               int64_t max_units, int64_t *n_units);
+
+/*
+ * Measurement hook: when `device_buffer` is not NULL, every later gemm_run of
+ * this plan writes four %globaltimer stamps (uint64 nanoseconds) per CTA into
+ * it: CTA start, prologue done, last operand copy issued, CTA end; CTA c at
+ * index 4*c.  It must hold at least 4 * 8 * GEMM_INFO_GRID bytes, else no
+ * stamps are written.  The caller owns the buffer.  NULL turns stamps off.
+ * Used to measure the idle time of SMs at the wave tail of each schedule.
+ * Errors: INVALID_ARG (NULL plan or a buffer not 8-byte aligned).
+ */
+gemm_status_t gemm_plan_set_trace(gemm_plan_t plan, void *device_buffer, size_t bytes);
 
 /* Tile coordinates (tile row, tile column) of raster id `tile` (issue, final
  * version, swizzle_tile / linear_tile).  Errors: INVALID_ARG. */

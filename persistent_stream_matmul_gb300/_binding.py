@@ -53,6 +53,7 @@ SIGNATURES = {
     "gemm_plan_units": (_i32, [_vp, _i64, ctypes.POINTER(ctypes.c_int32), _i64,
                                ctypes.POINTER(_i64)]),
     "gemm_plan_tile_coords": (_i32, [_vp, _i64, ctypes.POINTER(_i64), ctypes.POINTER(_i64)]),
+    "gemm_plan_set_trace": (_i32, [_vp, _vp, ctypes.c_size_t]),
     "gemm_plan_destroy": (_i32, [_vp]),
     "gemm_status_string": (ctypes.c_char_p, [_i32]),
 }
@@ -180,6 +181,11 @@ def gemm_plan_tile_coords(plan, tile: int):
     return tm.value, tn.value
 
 
+def gemm_plan_set_trace(plan, device_buffer, nbytes: int):
+    """Per-CTA %globaltimer stamps (start, ready, loads done, end) into a device buffer."""
+    _check(load().gemm_plan_set_trace(plan, _addr(device_buffer), nbytes), "gemm_plan_set_trace")
+
+
 def gemm_plan_destroy(plan):
     _check(load().gemm_plan_destroy(plan), "gemm_plan_destroy")
 
@@ -226,6 +232,9 @@ class Plan:
 
     def run_host(self, hA, hB, hC, dA, dB, dC, workspace=None, stream=None):
         gemm_run_host(self.handle, hA, hB, hC, dA, dB, dC, workspace, stream)
+
+    def set_trace(self, device_buffer, nbytes):
+        gemm_plan_set_trace(self.handle, device_buffer, nbytes)
 
     def last_status(self, stream=None) -> int:
         return gemm_last_status(self.handle, stream)

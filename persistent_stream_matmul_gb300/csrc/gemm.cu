@@ -72,6 +72,8 @@ struct gemm_plan {
     CUtensorMap tmA, tmB;
     const void* flags_cleared_for;
     bool attr_set[8];
+    unsigned long long* trace;  // optional per-CTA stamps (caller-owned device buffer)
+    size_t trace_bytes;
 };
 
 namespace {
@@ -484,6 +486,7 @@ gemm_status_t gemm_run(gemm_plan_t p, const void* A, const void* B, void* C, voi
     kp.inject_skip_cta = p->inject_skip;
     kp.wait_limit_ns = (uint64_t)p->wait_limit_us * 1000ull;
     kp.pipe_limit_ns = 4000000000ull;
+    kp.trace = (p->trace && p->trace_bytes >= (size_t)p->ctas * TRACE_N * 8) ? p->trace : nullptr;
 
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3((unsigned)p->ctas, 1, 1);
@@ -499,17 +502,17 @@ gemm_status_t gemm_run(gemm_plan_t p, const void* A, const void* B, void* C, voi
         attr[na].val.clusterDim.z = 1;
         ++na;
     }
-    // Stream-K CTAs wait on one another, so all must be resident at once.
-    // Without clusters a cooperative launch guarantees it.  Cluster launches
-    // are never made cooperative: their grid is sized to the number of
-    // clusters that fit at once (cudaOccupancyMaxActiveClusters), and the
-    // owners' waits are bounded, so a peer that is not resident turns into
-    // GEMM_ERR_TIMEOUT rather than a hang.
-    if (p->schedule == GEMM_SCHED_STREAMK && p->CM == 1) {
-        attr[na].id = cudaLaunchAttributeCooperative;
-        attr[na].val.cooperative = 1;
-        ++na;
-    }
+    // Programmatic dependent launch: this grid may start while the previous
+    // kernel in the stream drains; the kernel waits (griddepcontrol.wait)
+    // before touching global memory.
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+    // Stream-K owners wait on peers with higher CTA indices, which never
+    // wait themselves.  The grid is at most one CTA per SM (one CTA fits per
+    // SM; cluster grids are sized to cudaOccupancyMaxActiveClusters), so every
+    // peer gets an SM once the GPU has room, and the waits are bounded: a
+    // peer that cannot run in time turns into GEMM_ERR_TIMEOUT, never a hang.
     cfg.attrs = attr;
     cfg.numAttrs = na;
     void* args[3] = {&p->tmA, &p->tmB, &kp};
@@ -583,6 +586,13 @@ gemm_status_t gemm_plan_units(gemm_plan_t p, int64_t cta, int32_t* units, int64_
         ++n;
     }
     *n_units = n;
+    return GEMM_OK;
+}
+
+gemm_status_t gemm_plan_set_trace(gemm_plan_t p, void* device_buffer, size_t bytes) {
+    if (!p || (device_buffer && ((uintptr_t)device_buffer & 7u))) return GEMM_ERR_INVALID_ARG;
+    p->trace = reinterpret_cast<unsigned long long*>(device_buffer);
+    p->trace_bytes = device_buffer ? bytes : 0;
     return GEMM_OK;
 }
 

@@ -83,7 +83,13 @@ struct KParams {
     int32_t inject_skip_cta;     // test hook, -1 = off
     uint64_t wait_limit_ns;      // owner's wait for its peers
     uint64_t pipe_limit_ns;      // any wait inside the CTA's own pipeline
+    unsigned long long* trace;   // optional: 4 %globaltimer stamps per CTA, or null
 };
+
+// Per-CTA trace stamps (nanoseconds of %globaltimer): start of the CTA,
+// prologue done (after the wait for earlier grids), last copy issued by the
+// producer, CTA end (all epilogue stores issued).
+enum : int { TRACE_START = 0, TRACE_READY = 1, TRACE_LOADS_DONE = 2, TRACE_END = 3, TRACE_N = 4 };
 
 __device__ __forceinline__ void record_status(int* status, int code) {
     atomicCAS(status, 0, code);
@@ -169,6 +175,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int cta = blockIdx.x;                      // workspace slot of this CTA
+    const uint64_t t_start = globaltimer_ns();
     const int unit_cta = blockIdx.x / CM;            // index the scheduler knows
     const int rank = CM == 2 ? (int)cluster_ctarank() : 0;
 
@@ -201,6 +208,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
+
+    // Everything above touches only this CTA's shared and tensor memory, so
+    // it may overlap the previous kernel in the stream; global memory (A, B,
+    // C, workspace, status) is touched only after that kernel has finished.
+    grid_dependency_wait();
+    if (threadIdx.x == 0) {
+        grid_launch_dependents();
+        if (p.trace) {
+            p.trace[(size_t)cta * TRACE_N + TRACE_START] = t_start;
+            p.trace[(size_t)cta * TRACE_N + TRACE_READY] = globaltimer_ns();
+        }
+    }
 
     auto fail_pipe = [&]() {
         *abort_flag = 1;
@@ -273,6 +292,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     }
                 }
             }
+            if (p.trace) p.trace[(size_t)cta * TRACE_N + TRACE_LOADS_DONE] = globaltimer_ns();
             // before the CTA (or its peer) exits: every copy into this CTA has
             // landed, and every MMA that reads this CTA's ring (the peer's too)
             // has released it
@@ -466,6 +486,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     } else {
         __syncthreads();
     }
+    if (p.trace && threadIdx.x == 0) p.trace[(size_t)cta * TRACE_N + TRACE_END] = globaltimer_ns();
     if (warp == 1) {
         __syncwarp();
         tc_fence_after_sync();

@@ -22,6 +22,19 @@ __device__ __forceinline__ uint32_t elect_lane0() {
     return (threadIdx.x & 31) == 0;
 }
 
+// ---------------------------------------------------------------- dependent launch
+// Wait until the grids this launch depends on (earlier kernels in the stream)
+// have completed and their memory is visible.
+__device__ __forceinline__ void grid_dependency_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Allow the next grid in the stream to start launching (its CTAs land as this
+// grid's CTAs leave their SMs, and wait in grid_dependency_wait).
+__device__ __forceinline__ void grid_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");

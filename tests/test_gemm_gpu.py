@@ -205,6 +205,24 @@ def test_timeout_with_clusters_hits_only_the_silent_half():
     p.close()
 
 
+@pytest.mark.parametrize("sched", SCHEDS)
+def test_trace_stamps_are_ordered(sched):
+    M, N, K, dtype = 1024, 1536, 1024, inputs.BF16
+    A, Bm, dA, dB = _case(M, N, K, dtype, 0, 1, ("normal", 1.0), 14)
+    p = B.Plan(M, N, K, dtype, 0, 1, sched)
+    ctas = p.info("grid")
+    buf = torch.zeros(4 * ctas, dtype=torch.int64, device="cuda")
+    p.set_trace(buf, buf.numel() * 8)
+    Cb = run(p, dA, dB, M, N)
+    _check_full(Cb, A, Bm, M, N, K, dtype, 0, 1)
+    t = buf.cpu().numpy().reshape(ctas, 4)
+    assert (t > 0).all()
+    assert (t[:, 0] <= t[:, 1]).all() and (t[:, 1] <= t[:, 2]).all() and (t[:, 2] <= t[:, 3]).all()
+    assert t[:, 3].max() - t[:, 0].min() < 10_000_000_000   # one run, well under 10 s
+    p.set_trace(None, 0)
+    p.close()
+
+
 def test_run_host_end_to_end():
     M, N, K, dtype = 256, 384, 640, inputs.BF16
     A, Bm = inputs.operands(M, N, K, dtype, 0, 1, ("normal", 1.0), ("normal", 1.0), 12)
