@@ -19,6 +19,11 @@
  *                             whole tiles.  Split tiles are fixed up through
  *                             a fp32 workspace and per-tile flags, in a fixed
  *                             order, so results are deterministic.
+ *   GEMM_SCHED_SPLITK         fixed split-K (the issue's closing comments name
+ *                             it as the alternative decomposition): every
+ *                             tile's K range is cut into S near-equal parts
+ *                             (GEMM_OPT_SPLIT_K), computed by a persistent
+ *                             grid and fixed up like Stream-K.
  *
  * Conventions for every entry point:
  *  - Each call returns a gemm_status_t; nothing else crosses the ABI.  An
@@ -55,7 +60,8 @@ typedef enum { GEMM_ROW_MAJOR = 0, GEMM_COL_MAJOR = 1 } gemm_layout_t;
 typedef enum {
     GEMM_SCHED_DATA_PARALLEL = 0,
     GEMM_SCHED_PERSISTENT = 1,
-    GEMM_SCHED_STREAMK = 2
+    GEMM_SCHED_STREAMK = 2,
+    GEMM_SCHED_SPLITK = 3
 } gemm_schedule_t;
 
 typedef enum {
@@ -84,8 +90,9 @@ enum {
      * the linear raster.  Default 8 for PERSISTENT and STREAMK, 0 for
      * DATA_PARALLEL. */
     GEMM_OPT_GROUP_M = 2,
-    /* output tile width BN: 128 or 256; 0 (default) lets the plan choose.
-     * The tile height is 128 rows and the k-slice 64. */
+    /* output tile width BN: 64, 128 or 256; 0 (default) lets the plan
+     * choose.  The tile height is 128 rows and the k-slice 64.  64-wide tiles
+     * run without clusters (GEMM_OPT_CLUSTER_M = 2 with them is UNSUPPORTED). */
     GEMM_OPT_TILE_N = 3,
     /* 1 (default): the issue's "two_tiles" rule adds g more Stream-K tiles
      * when more than g whole tiles would remain; 0: sk = tiles mod g. */
@@ -102,7 +109,23 @@ enum {
      * it to both).  0 (default) lets the plan choose (2 for wide tiles with at
      * least two row tiles).  With 2, the scheduler's tiles are 256 rows tall,
      * GEMM_OPT_GRID counts CTAs (pairs of them form one scheduling unit). */
-    GEMM_OPT_CLUSTER_M = 7
+    GEMM_OPT_CLUSTER_M = 7,
+    /* Stream-K tile count: 0 (default) = the hybrid rule of the issue's final
+     * version (tiles mod g, plus g under GEMM_OPT_TWO_TILES; the rest are whole
+     * tiles); 1 = every tile goes to the Stream-K wave (the iteration space of
+     * the whole product is split evenly over the g CTAs). */
+    GEMM_OPT_SK_MODE = 8,
+    /* split-K parts per tile for GEMM_SCHED_SPLITK; 0 (default) = as many
+     * as fit in one round of the grid, floor(units / tiles), at least 1 and
+     * at most ceil(K/64)/4. */
+    GEMM_OPT_SPLIT_K = 9,
+    /* k order of whole tiles: 1 = tile t starts at k-block t*ipt/tiles and
+     * wraps around (changes only the fp32 summation order of those tiles),
+     * 0 (default) = ascending. */
+    GEMM_OPT_K_ROTATE = 10,
+    /* k-blocks of B prefetched into L2 ahead of the shared-memory ring
+     * (0 = off, the default; up to 256). */
+    GEMM_OPT_L2_PREFETCH = 11
 };
 
 /* Keys for gemm_plan_get_info. */
@@ -119,7 +142,11 @@ enum {
     GEMM_INFO_STAGES = 13,          /* depth of the shared-memory ring */
     GEMM_INFO_GROUP_M = 14,
     GEMM_INFO_SMEM_BYTES = 15,      /* dynamic shared memory per CTA */
-    GEMM_INFO_CLUSTER_M = 16        /* CTAs per cluster (1 or 2) */
+    GEMM_INFO_CLUSTER_M = 16,       /* CTAs per cluster (1 or 2) */
+    GEMM_INFO_A_ROWS_PER_STAGE = 17,/* rows of A each ring stage loads: 128, or 64 when M <= 64 */
+    GEMM_INFO_SPLIT_K = 18,         /* split-K parts per tile (0 unless GEMM_SCHED_SPLITK) */
+    GEMM_INFO_K_ROTATE = 19,        /* 1 when whole tiles rotate their k order */
+    GEMM_INFO_L2_PREFETCH = 20      /* k-blocks of B prefetched into L2 ahead of the ring */
 };
 
 /* Roles of a work unit reported by gemm_plan_units. */
@@ -155,9 +182,11 @@ gemm_status_t gemm_plan_get_info(gemm_plan_t plan, int key, int64_t *value);
 
 /*
  * Bytes of device workspace gemm_run needs: 0 for DATA_PARALLEL and
- * PERSISTENT; for STREAMK, 8 bytes of flag per split tile (rounded up to 256)
- * plus one 128 x BN fp32 partial-tile slot per CTA (the "scratchpad" of the
- * Stream-K fixup mentioned in the issue, second code version).
+ * PERSISTENT; for STREAMK, 8 bytes of flag per split tile and cluster half
+ * (rounded up to 256) plus one 128 x BN fp32 partial-tile slot per CTA (the
+ * "scratchpad" of the Stream-K fixup mentioned in the issue, second code
+ * version); for SPLITK, a flag per tile and half plus a slot per tile, part
+ * beyond the first, and half.
  * The caller allocates it (16-byte aligned) and owns it; the plan clears the
  * flag part the first time it sees a workspace address.  Errors: INVALID_ARG.
  */

@@ -24,7 +24,9 @@ Where the page leaves a step open, the reading is:
   segment holding the last iteration store and the others add atomically);
 * a persistent program that finishes its Stream-K range goes on with whole
   tiles ``sk + pid, sk + pid + g, ...`` (the page launches them as a second
-  grid); the set of whole tiles is the same.
+  grid); the set of whole tiles is the same;
+* ``all_streamk``: every tile goes to the Stream-K wave (``sk = tiles``), the
+  plain form of splitting the whole iteration space evenly over the programs.
 """
 from __future__ import annotations
 
@@ -46,6 +48,7 @@ class Schedule:
     g: int                  # programs in the Stream-K wave (0: no Stream-K)
     two_tiles: bool = True
     group_m: int = 8        # 0 selects the linear raster
+    all_streamk: bool = False
     tiles_m: int = field(init=False)
     tiles_n: int = field(init=False)
     tiles: int = field(init=False)
@@ -65,6 +68,8 @@ class Schedule:
             sk = self.tiles % self.g
             if self.two_tiles and self.tiles - sk > self.g:
                 sk += self.g
+            if self.all_streamk:
+                sk = self.tiles
             self.sk_tiles = sk
             self.dp_tiles = self.tiles - sk
             self.sk_iters = sk * self.ipt
@@ -121,3 +126,11 @@ class Schedule:
             gsize = min(tm - gid * G, G)
             return gid * G + tile % gsize, (tile % width) // gsize
         return tile // tn, tile % tn
+
+
+def splitk_parts(ipt: int, S: int):
+    """k-ranges of a fixed split of one tile's ``ipt`` iterations into ``S``
+    parts (the issue's closing comments name split-K as the alternative
+    decomposition but print no formula; reading: near-equal contiguous parts,
+    part p = [floor(p*ipt/S), floor((p+1)*ipt/S)), the first one the owner)."""
+    return [(p * ipt // S, (p + 1) * ipt // S) for p in range(S)]

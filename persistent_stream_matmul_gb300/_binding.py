@@ -16,8 +16,8 @@ LIB_PATH = os.path.join(HERE, "libpsm_gemm.so")
 
 GEMM_F16, GEMM_BF16 = 0, 1
 GEMM_ROW_MAJOR, GEMM_COL_MAJOR = 0, 1
-GEMM_SCHED_DATA_PARALLEL, GEMM_SCHED_PERSISTENT, GEMM_SCHED_STREAMK = 0, 1, 2
-SCHEDULES = {"dp": 0, "persistent": 1, "streamk": 2}
+GEMM_SCHED_DATA_PARALLEL, GEMM_SCHED_PERSISTENT, GEMM_SCHED_STREAMK, GEMM_SCHED_SPLITK = 0, 1, 2, 3
+SCHEDULES = {"dp": 0, "persistent": 1, "streamk": 2, "splitk": 3}
 
 (GEMM_OK, GEMM_ERR_INVALID_ARG, GEMM_ERR_UNSUPPORTED, GEMM_ERR_WORKSPACE, GEMM_ERR_CUDA,
  GEMM_ERR_LAUNCH, GEMM_ERR_TIMEOUT, GEMM_ERR_NO_DEVICE) = range(8)
@@ -29,11 +29,17 @@ GEMM_OPT_TWO_TILES = 4
 GEMM_OPT_WAIT_LIMIT_US = 5
 GEMM_OPT_INJECT_SKIP_POST = 6
 GEMM_OPT_CLUSTER_M = 7
+GEMM_OPT_SK_MODE = 8
+GEMM_OPT_SPLIT_K = 9
+GEMM_OPT_K_ROTATE = 10
+GEMM_OPT_L2_PREFETCH = 11
 
 INFO = {
     "tile_m": 1, "tile_n": 2, "tile_k": 3, "tiles_m": 4, "tiles_n": 5, "tiles": 6,
     "iters_per_tile": 7, "grid": 8, "sk_tiles": 9, "sk_iters_per_cta": 10,
     "sk_iters_rem": 11, "num_sms": 12, "stages": 13, "group_m": 14, "smem_bytes": 15, "cluster_m": 16,
+    "a_rows_per_stage": 17, "split_k": 18, "k_rotate": 19,
+    "l2_prefetch": 20,
 }
 ROLE_FULL, ROLE_OWNER, ROLE_PEER = 0, 1, 2
 
@@ -206,7 +212,9 @@ class Plan:
                                                    offline_sms)
         keys = {"grid": GEMM_OPT_GRID, "group_m": GEMM_OPT_GROUP_M, "tile_n": GEMM_OPT_TILE_N,
                 "two_tiles": GEMM_OPT_TWO_TILES, "wait_limit_us": GEMM_OPT_WAIT_LIMIT_US,
-                "inject_skip_post": GEMM_OPT_INJECT_SKIP_POST, "cluster_m": GEMM_OPT_CLUSTER_M}
+                "inject_skip_post": GEMM_OPT_INJECT_SKIP_POST, "cluster_m": GEMM_OPT_CLUSTER_M,
+                "sk_mode": GEMM_OPT_SK_MODE, "split_k": GEMM_OPT_SPLIT_K,
+                "k_rotate": GEMM_OPT_K_ROTATE, "l2_prefetch": GEMM_OPT_L2_PREFETCH}
         for k, v in options.items():
             if v is not None:
                 gemm_plan_set_option(self.handle, keys[k], int(v))

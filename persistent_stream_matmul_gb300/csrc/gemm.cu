@@ -56,11 +56,12 @@ struct gemm_plan {
     int dtype, layout_a, layout_b, schedule;
     int device, num_sms, offline;
     // options
-    int opt_grid, opt_group_m, opt_tile_n, opt_two_tiles, inject_skip, opt_cluster_m;
+    int opt_grid, opt_group_m, opt_tile_n, opt_two_tiles, inject_skip, opt_cluster_m, opt_sk_mode;
+    int opt_split, opt_k_rotate, opt_l2_prefetch;
     int64_t wait_limit_us;
     int max_pair_ctas;  // CTAs co-resident as 2-CTA clusters (0: unknown)
     // derived
-    int BN, CM, ctas, stages, smem_bytes;
+    int BN, CM, AROWS, ctas, stages, smem_bytes;
     Sched s;
     size_t ws_flag_bytes, ws_bytes;
     // device state
@@ -71,7 +72,7 @@ struct gemm_plan {
     bool tm_valid;
     CUtensorMap tmA, tmB;
     const void* flags_cleared_for;
-    bool attr_set[8];
+    bool attr_set[16];
     unsigned long long* trace;  // optional per-CTA stamps (caller-owned device buffer)
     size_t trace_bytes;
 };
@@ -80,12 +81,12 @@ namespace {
 
 bool valid_enums(int dtype, int la, int lb, int sched) {
     return (dtype == GEMM_F16 || dtype == GEMM_BF16) && (la == 0 || la == 1) &&
-           (lb == 0 || lb == 1) && (sched >= 0 && sched <= 2);
+           (lb == 0 || lb == 1) && (sched >= 0 && sched <= 3);
 }
 
-template <int BN, bool BF, int CM>
+template <int BN, bool BF, int CM, int AROWS = 128>
 void* kernel_ptr() {
-    return reinterpret_cast<void*>(&gemm_kernel<BN, BF, CM>);
+    return reinterpret_cast<void*>(&gemm_kernel<BN, BF, CM, AROWS>);
 }
 
 template <int CM>
@@ -95,16 +96,34 @@ void* pick_kernel_cm(int BN, int dtype) {
     return dtype == GEMM_BF16 ? kernel_ptr<128, true, CM>() : kernel_ptr<128, false, CM>();
 }
 
-void* pick_kernel(int BN, int dtype, int CM) {
+void* pick_kernel(int BN, int dtype, int CM, int AROWS = 128) {
+    const bool bf = dtype == GEMM_BF16;
+    if (BN == 64) {  // only with CM = 1
+        if (AROWS == 64) return bf ? kernel_ptr<64, true, 1, 64>() : kernel_ptr<64, false, 1, 64>();
+        return bf ? kernel_ptr<64, true, 1>() : kernel_ptr<64, false, 1>();
+    }
+    if (AROWS == 64)  // BN = 128, CM = 1
+        return bf ? kernel_ptr<128, true, 1, 64>() : kernel_ptr<128, false, 1, 64>();
     return CM == 2 ? pick_kernel_cm<2>(BN, dtype) : pick_kernel_cm<1>(BN, dtype);
 }
 
-int kernel_index(int BN, int dtype, int CM) {
-    return (BN == 256 ? 4 : 0) + (dtype == GEMM_BF16 ? 2 : 0) + (CM == 2 ? 1 : 0);
+int kernel_index(int BN, int dtype, int CM, int AROWS) {
+    const int bf = dtype == GEMM_BF16 ? 1 : 0;
+    if (BN == 64) return 10 + 2 * (AROWS == 64 ? 1 : 0) + bf;
+    if (AROWS == 64) return 8 + bf;
+    return (BN == 256 ? 4 : 0) + 2 * bf + (CM == 2 ? 1 : 0);
 }
 
-int smem_for(int BN) { return BN == 256 ? Cfg<256>::SMEM_BYTES : Cfg<128>::SMEM_BYTES; }
-int stages_for(int BN) { return BN == 256 ? Cfg<256>::STAGES : Cfg<128>::STAGES; }
+int smem_for(int BN, int AROWS = 128) {
+    if (BN == 64) return AROWS == 64 ? Cfg<64, 64>::SMEM_BYTES : Cfg<64>::SMEM_BYTES;
+    if (AROWS == 64) return Cfg<128, 64>::SMEM_BYTES;
+    return BN == 256 ? Cfg<256>::SMEM_BYTES : Cfg<128>::SMEM_BYTES;
+}
+int stages_for(int BN, int AROWS = 128) {
+    if (BN == 64) return AROWS == 64 ? Cfg<64, 64>::STAGES : Cfg<64>::STAGES;
+    if (AROWS == 64) return Cfg<128, 64>::STAGES;
+    return BN == 256 ? Cfg<256>::STAGES : Cfg<128>::STAGES;
+}
 
 // Derive the tile grid and the schedule from the shape and the options
 // (issue "Stream-k matmul implementation very slow ...", final version,
@@ -112,15 +131,26 @@ int stages_for(int BN) { return BN == 256 ? Cfg<256>::STAGES : Cfg<128>::STAGES;
 // split of the Stream-K iterations).
 gemm_status_t derive(gemm_plan* p) {
     const int64_t tiles_m128 = cdiv64(p->M, BM);
+    // Tile width: 256 when that still gives every SM a tile (compute-bound
+    // shapes: fewest operand bytes per FLOP); 64 for small problems with
+    // several rows of tiles that would leave most SMs idle at 128 (more tiles
+    // instead of a split of K); else 128.  A single row of tiles streams a B
+    // that is read once and keeps 128: 256-byte runs per row of a row-major B
+    // stream about twice as fast as 128-byte ones.
     int BN = p->opt_tile_n;
     if (BN == 0) {
         const int64_t tiles256 = tiles_m128 * cdiv64(p->N, 256);
-        BN = (p->N > 128 && tiles256 >= p->num_sms) ? 256 : 128;
+        const int64_t tiles128 = tiles_m128 * cdiv64(p->N, 128);
+        if (p->N > 128 && tiles256 >= p->num_sms) BN = 256;
+        else if (p->N <= 64 || (tiles_m128 >= 2 && 2 * tiles128 < p->num_sms)) BN = 64;
+        else BN = 128;
+        if (BN == 64 && p->opt_cluster_m == 2) BN = 128;  // clusters need 128+ wide tiles
     }
     // 2-CTA clusters share B between two 128-row halves: worth it when there
     // are at least two row tiles and the tile is wide (compute-bound shapes)
     int CM = p->opt_cluster_m;
     if (CM == 0) CM = (tiles_m128 >= 2 && BN == 256) ? 2 : 1;
+    if (BN == 64 && CM == 2) return GEMM_ERR_UNSUPPORTED;  // 64-wide tiles run without clusters
     // the scheduler works on tiles of CM*128 rows and on units of CM CTAs
     const int64_t tiles_m = cdiv64(p->M, (int64_t)BM * CM);
     const int64_t tiles_n = cdiv64(p->N, BN);
@@ -146,9 +176,24 @@ gemm_status_t derive(gemm_plan* p) {
     } else if (p->schedule == GEMM_SCHED_PERSISTENT) {
         s.grid = (int32_t)(tiles < g ? tiles : g);
         s.persistent = 1;
+    } else if (p->schedule == GEMM_SCHED_SPLITK) {
+        // as many parts as fit in one round of the scheduling units, at most
+        // one part per 4 k-iterations
+        int64_t S = p->opt_split;
+        if (S == 0) {
+            S = tiles >= g ? 1 : g / tiles;
+            const int64_t cap = ipt / 4 > 1 ? ipt / 4 : 1;
+            if (S > cap) S = cap;
+        }
+        if (S > ipt) S = ipt > 0 ? ipt : 1;
+        if (tiles * S > INT32_MAX / 2) return GEMM_ERR_UNSUPPORTED;
+        s.split = (int32_t)S;
+        s.grid = (int32_t)(tiles * S < g ? tiles * S : g);
+        s.persistent = 1;
     } else {
         int64_t sk = tiles % g;
         if (p->opt_two_tiles && tiles - sk > g) sk += g;
+        if (p->opt_sk_mode == 1) sk = tiles;  // every tile in the Stream-K wave
         s.sk_tiles = (int32_t)sk;
         s.grid = tiles > 0 ? g : 0;
         s.persistent = 1;
@@ -156,15 +201,25 @@ gemm_status_t derive(gemm_plan* p) {
         s.sk_q = iters / g;
         s.sk_r = iters % g;
     }
+    s.k_rotate = p->opt_k_rotate > 0 ? 1 : 0;
+    // off by default: measured slower on a B read once (extra L2 requests)
+    s.l2_prefetch = p->opt_l2_prefetch > 0 ? p->opt_l2_prefetch : 0;
     p->s = s;
     p->BN = BN;
     p->CM = CM;
+    // one row of tiles with at most 64 valid rows: load only those rows of A
+    p->AROWS = (p->M <= 64 && CM == 1 && BN <= 128) ? 64 : 128;
     p->ctas = s.grid * CM;
-    p->stages = stages_for(BN);
-    p->smem_bytes = smem_for(BN);
+    p->stages = stages_for(BN, p->AROWS);
+    p->smem_bytes = smem_for(BN, p->AROWS);
     if (p->schedule == GEMM_SCHED_STREAMK && s.sk_tiles > 0) {
         p->ws_flag_bytes = ((size_t)s.sk_tiles * CM * 8 + 255) / 256 * 256;
         p->ws_bytes = p->ws_flag_bytes + (size_t)p->ctas * BM * BN * sizeof(float);
+    } else if (p->schedule == GEMM_SCHED_SPLITK && s.split > 1) {
+        // one flag per tile half, one partial slot per (tile, part >= 1, half)
+        p->ws_flag_bytes = ((size_t)s.tiles * CM * 8 + 255) / 256 * 256;
+        p->ws_bytes = p->ws_flag_bytes +
+                      (size_t)s.tiles * (s.split - 1) * CM * BM * BN * sizeof(float);
     } else {
         p->ws_flag_bytes = 0;
         p->ws_bytes = 0;
@@ -227,6 +282,10 @@ gemm_status_t make_plan(gemm_plan_t* out, int64_t M, int64_t N, int64_t K, int d
     p->opt_two_tiles = 1;
     p->inject_skip = -1;
     p->opt_cluster_m = 0;
+    p->opt_sk_mode = 0;
+    p->opt_split = 0;
+    p->opt_k_rotate = 0;
+    p->opt_l2_prefetch = -1;
     p->wait_limit_us = 1000000;
     if (offline) {
         if (num_sms <= 0) { delete p; return GEMM_ERR_INVALID_ARG; }
@@ -292,7 +351,7 @@ gemm_status_t encode_maps(gemm_plan* p, const void* A, const void* B) {
         if (p->layout_a == GEMM_ROW_MAJOR) {
             dims[0] = (cuuint64_t)p->K; dims[1] = (cuuint64_t)p->M;
             strides[0] = (cuuint64_t)p->K * 2;
-            box[0] = BK; box[1] = BM;
+            box[0] = BK; box[1] = (cuuint32_t)p->AROWS;
         } else {
             dims[0] = (cuuint64_t)p->M; dims[1] = (cuuint64_t)p->K;
             strides[0] = (cuuint64_t)p->M * 2;
@@ -372,7 +431,7 @@ gemm_status_t gemm_plan_set_option(gemm_plan_t p, int key, int64_t value) {
             p->opt_group_m = (int)value;
             break;
         case GEMM_OPT_TILE_N:
-            if (value != 0 && value != 128 && value != 256) return GEMM_ERR_UNSUPPORTED;
+            if (value != 0 && value != 64 && value != 128 && value != 256) return GEMM_ERR_UNSUPPORTED;
             p->opt_tile_n = (int)value;
             break;
         case GEMM_OPT_TWO_TILES:
@@ -390,6 +449,22 @@ gemm_status_t gemm_plan_set_option(gemm_plan_t p, int key, int64_t value) {
         case GEMM_OPT_CLUSTER_M:
             if (value != 0 && value != 1 && value != 2) return GEMM_ERR_UNSUPPORTED;
             p->opt_cluster_m = (int)value;
+            break;
+        case GEMM_OPT_SK_MODE:
+            if (value != 0 && value != 1) return GEMM_ERR_UNSUPPORTED;
+            p->opt_sk_mode = (int)value;
+            break;
+        case GEMM_OPT_SPLIT_K:
+            if (value < 0 || value > 4096) return GEMM_ERR_UNSUPPORTED;
+            p->opt_split = (int)value;
+            break;
+        case GEMM_OPT_K_ROTATE:
+            if (value < 0 || value > 1) return GEMM_ERR_UNSUPPORTED;
+            p->opt_k_rotate = (int)value;
+            break;
+        case GEMM_OPT_L2_PREFETCH:
+            if (value < 0 || value > 256) return GEMM_ERR_UNSUPPORTED;
+            p->opt_l2_prefetch = (int)value;
             break;
         default:
             return GEMM_ERR_INVALID_ARG;
@@ -419,6 +494,10 @@ gemm_status_t gemm_plan_get_info(gemm_plan_t p, int key, int64_t* value) {
         case GEMM_INFO_GROUP_M: v = p->s.group_m; break;
         case GEMM_INFO_SMEM_BYTES: v = p->smem_bytes; break;
         case GEMM_INFO_CLUSTER_M: v = p->CM; break;
+        case GEMM_INFO_A_ROWS_PER_STAGE: v = p->AROWS; break;
+        case GEMM_INFO_SPLIT_K: v = p->s.split; break;
+        case GEMM_INFO_K_ROTATE: v = p->s.k_rotate; break;
+        case GEMM_INFO_L2_PREFETCH: v = p->s.l2_prefetch; break;
         default: return GEMM_ERR_INVALID_ARG;
     }
     *value = v;
@@ -454,8 +533,8 @@ gemm_status_t gemm_run(gemm_plan_t p, const void* A, const void* B, void* C, voi
     gemm_status_t es = encode_maps(p, A, B);
     if (es != GEMM_OK) return es;
 
-    void* fn = pick_kernel(p->BN, p->dtype, p->CM);
-    const int bi = kernel_index(p->BN, p->dtype, p->CM);
+    void* fn = pick_kernel(p->BN, p->dtype, p->CM, p->AROWS);
+    const int bi = kernel_index(p->BN, p->dtype, p->CM, p->AROWS);
     if (!p->attr_set[bi]) {
         if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, p->smem_bytes) !=
             cudaSuccess)

@@ -51,22 +51,31 @@ constexpr int UMMA_K = 16;           // k of one tcgen05.mma kind::f16
 constexpr int NUM_THREADS = 192;
 constexpr int EPI_WARP0 = 2;         // first epilogue warp
 constexpr int EPI_THREADS = 128;
-constexpr int A_STAGE_BYTES = BM * BK * 2;
 constexpr int SW_ATOM_BYTES = 1024;  // 8 rows x 128 B
 constexpr int MN_CHUNK_BYTES = 64 * BK * 2;  // one 64-element-wide MN-major box (8 KB)
 
 enum : int { STATUS_OK = 0, STATUS_FLAG_TIMEOUT = 1, STATUS_PIPE_TIMEOUT = 2 };
 enum : uint32_t { BAR_EPI_SYNC = 1, BAR_EPI_VOTE = 2 };  // named barriers (0 = __syncthreads)
 
-template <int BN>
+// AROWS: rows of A loaded per stage.  128 normally.  64 when M <= 64: the
+// MMA still reads 128 rows, and rows 64-127 alias the first bytes of the
+// stage's B tile, so those accumulator rows hold garbage that is never stored
+// (each output row depends only on its own row of A); the smaller stage lets
+// the ring hold more B in flight.
+template <int BN, int AROWS = 128>
 struct Cfg {
+    static constexpr int A_STAGE_BYTES = AROWS * BK * 2;
     static constexpr int B_STAGE_BYTES = BN * BK * 2;
     static constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
-    static constexpr int STAGES = BN == 256 ? 4 : 6;
+    static constexpr int STAGES_FIT = (192 * 1024) / STAGE_BYTES;  // 4, 6, 8 or 12
+    static constexpr int STAGES = STAGES_FIT > 12 ? 12 : STAGES_FIT;
     static constexpr int TMEM_COLS = 2 * BN;  // two accumulators; 256 or 512
     static constexpr int BAR_BYTES = 256;
     static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + BAR_BYTES + 1024;
-    static_assert(BN == 128 || BN == 256, "tile width");
+    static_assert(BN == 64 || BN == 128 || BN == 256, "tile width");
+    static_assert(AROWS == 128 || AROWS == 64, "rows of A per stage");
+    static_assert(AROWS == 128 || A_STAGE_BYTES + B_STAGE_BYTES >= BM * BK * 2,
+                  "the MMA's 128-row read of A must stay inside the stage");
     static_assert((2 * STAGES + 5) * 8 + 8 <= BAR_BYTES, "barrier area");
 };
 
@@ -148,11 +157,13 @@ __device__ __forceinline__ uint32_t pack2(float a, float b) {
     }
 }
 
-template <int BN, bool OUT_BF16, int CM>
+template <int BN, bool OUT_BF16, int CM, int AROWS = 128>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ KParams p) {
-    using Cf = Cfg<BN>;
+    using Cf = Cfg<BN, AROWS>;
+    static_assert(AROWS == 128 || CM == 1, "half-height A only without clusters");
+    static_assert(BN >= 128 || CM == 1, "64-wide tiles only without clusters");
     constexpr int STAGES = Cf::STAGES;
     static_assert(CM == 1 || CM == 2, "cluster size");
     constexpr uint16_t PAIR = 0x3;
@@ -243,7 +254,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             bool ok = true;
             while (ok && cursor_next(p.s, unit_cta, cur, u)) {
                 const int m0 = (u.tm * CM + rank) * BM, n0 = u.tn * BN;
-                for (int kb = u.k0; kb < u.k1; ++kb) {
+                const int nk = u.k1 - u.k0;
+                // L2 prefetch of B, l2_prefetch k-blocks ahead of the loads: keeps
+                // DRAM busy beyond what the shared-memory ring can hold in flight
+                const int pf = p.s.l2_prefetch;
+                auto prefetch_b = [&](int step) {
+                    const int kp = unit_kblock(p.s, u.tile, u.k0, u.k1, step) * BK;
+                    if (!p.b_mn) {
+                        tma_prefetch_l2_2d(&tmB, kp, n0 + rank * (BN / CM));
+                    } else {
+#pragma unroll
+                        for (int c = rank * (BN / 64) / CM; c < (rank + 1) * (BN / 64) / CM; ++c)
+                            tma_prefetch_l2_2d(&tmB, n0 + 64 * c, kp);
+                    }
+                };
+                for (int i = 0; i < pf && i < nk; ++i) prefetch_b(i);
+                for (int i = 0; i < nk; ++i) {
+                    const int kb = unit_kblock(p.s, u.tile, u.k0, u.k1, i);
+                    if (pf > 0 && i + pf < nk) prefetch_b(i + pf);
                     if (!mbar_wait(empty_bar(stage), phase ^ 1u, p.pipe_limit_ns)) {
                         fail_pipe();
                         ok = false;
@@ -252,14 +280,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     if (*abort_flag) { ok = false; break; }
                     const uint32_t fb = full_bar(stage);
                     const uint32_t sa = sbase + stage * Cf::STAGE_BYTES;
-                    const uint32_t sb = sa + A_STAGE_BYTES;
+                    const uint32_t sb = sa + Cf::A_STAGE_BYTES;
                     const int k_el = kb * BK;
                     mbar_arrive_expect_tx(fb, Cf::STAGE_BYTES);
                     if (!p.a_mn) {
-                        tma_load_2d(sa, &tmA, fb, k_el, m0, pol_a);
+                        tma_load_2d(sa, &tmA, fb, k_el, m0, pol_a);  // box of AROWS rows
                     } else {
 #pragma unroll
-                        for (int c = 0; c < BM / 64; ++c)
+                        for (int c = 0; c < AROWS / 64; ++c)
                             tma_load_2d(sa + c * MN_CHUNK_BYTES, &tmA, fb, m0 + 64 * c, k_el, pol_a);
                     }
                     if constexpr (CM == 1) {
@@ -319,7 +347,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
                 tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + (uint32_t)(buf * BN);
-                for (int kb = u.k0; kb < u.k1; ++kb) {
+                for (int i = 0; i < u.k1 - u.k0; ++i) {
                     if (!mbar_wait(full_bar(stage), phase, p.pipe_limit_ns)) {
                         fail_pipe();
                         ok = false;
@@ -328,7 +356,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     if (*abort_flag) { ok = false; break; }
                     tc_fence_after_sync();
                     const uint32_t sa = sbase + stage * Cf::STAGE_BYTES;
-                    const uint32_t sb = sa + A_STAGE_BYTES;
+                    const uint32_t sb = sa + Cf::A_STAGE_BYTES;
 #pragma unroll
                     for (int kk = 0; kk < BK / UMMA_K; ++kk) {
                         // K-major: a k-step of 16 elements is 32 bytes along the
@@ -339,7 +367,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         const uint64_t bdesc =
                             p.b_mn ? smem_desc_sw128(sb + kk * 16 * 128, MN_CHUNK_BYTES, SW_ATOM_BYTES)
                                    : smem_desc_sw128(sb + kk * UMMA_K * 2, 16, SW_ATOM_BYTES);
-                        mma_f16_ss(d_tmem, adesc, bdesc, p.idesc, (kb > u.k0 || kk > 0) ? 1u : 0u);
+                        mma_f16_ss(d_tmem, adesc, bdesc, p.idesc, (i > 0 || kk > 0) ? 1u : 0u);
                     }
                     if constexpr (CM == 2) {
                         mma_commit_multicast(empty_bar(stage), PAIR);  // both halves of B were read
@@ -385,7 +413,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if (u.role == ROLE_PEER) {
                 // fp32 partial -> this CTA's slot, laid out [chunk][vec][row] so
                 // a warp's 16-byte stores cover 512 contiguous bytes
-                float4* slot = reinterpret_cast<float4*>(p.partials + (size_t)cta * BM * BN);
+                float4* slot =
+                    reinterpret_cast<float4*>(p.partials + (size_t)(u.slot * CM + rank) * BM * BN);
 #pragma unroll 1
                 for (int j = 0; j < BN / 32; ++j) {
                     uint32_t r[32];
@@ -424,7 +453,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
                     for (int i = 0; i < 32; ++i) acc[i] = __uint_as_float(r[i]);
                     if (u.role == ROLE_OWNER && store && row_ok) {
-                        // peers in ascending k: the same half of units unit_cta+1 ..
+                        // peers in ascending k: slots u.slot, u.slot + 1, ... (this half)
                         // Loads of PEER_BATCH peers are issued before any of them is
                         // added, so 32 16-byte loads per thread are in flight; the
                         // additions keep the ascending order.
@@ -439,7 +468,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             for (int q = 0; q < PEER_BATCH; ++q) {
                                 if (pp + q <= u.npeers) {
                                     const float4* slot =
-                                        base + (size_t)((unit_cta + pp + q) * CM + rank) * slot_f4;
+                                        base + (size_t)((u.slot + pp - 1 + q) * CM + rank) * slot_f4;
 #pragma unroll
                                     for (int v = 0; v < 8; ++v) x[q][v] = ld_cg_f4(slot + (size_t)v * BM);
                                 }

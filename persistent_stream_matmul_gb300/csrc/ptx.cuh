@@ -112,6 +112,15 @@ __device__ __forceinline__ void tma_load_2d_multicast(uint32_t dst, const CUtens
         : "memory");
 }
 
+// Bring a box of a tensor into L2 only (no shared memory, no completion
+// signal): used to run far ahead of the ring for operands read once.
+__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int32_t x, int32_t y) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y)
+                 : "memory");
+}
+
 __device__ __forceinline__ uint32_t cluster_ctarank() {
     uint32_t r;
     asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));

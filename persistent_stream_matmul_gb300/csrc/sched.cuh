@@ -14,11 +14,20 @@
 // machinery with no Stream-K tiles and a grid of one CTA per SM; the
 // data-parallel schedule launches one CTA per tile.
 //
+// Split-K (GitHub issue above, closing comments: a fixed split of K as the
+// alternative decomposition): every tile's k-range is cut into `split`
+// near-equal parts; units are numbered part-major with the k = 0 parts (the
+// owners) last, and a persistent grid takes units c, c + grid, ...  A CTA
+// therefore finishes all its peer units before any owner unit, and owners
+// wait only on peers, which never wait.
+//
 // Fixup roles.  A unit that starts at k-iteration 0 of its tile and ends
 // before the tile's last iteration is the OWNER; a unit that starts past
 // iteration 0 is a PEER.  A CTA's range is contiguous, so only its first unit
 // can be a PEER and only its last can be an OWNER.  The peers of an owner in
-// CTA c are CTAs c+1 .. c+npeers, in ascending k.
+// CTA c are CTAs c+1 .. c+npeers, in ascending k.  Every unit carries the
+// partial-tile slot it writes (PEER) or the first slot it reads (OWNER); an
+// owner's peers occupy consecutive slots in ascending k.
 #pragma once
 #include <stdint.h>
 
@@ -39,6 +48,10 @@ struct Sched {
     int32_t grid;        // CTAs launched
     int32_t sk_tiles;    // raster ids [0, sk_tiles) are split by Stream-K
     int32_t persistent;  // 1: CTA c takes whole tiles sk+c, sk+c+grid, ...
+    int32_t split;       // split-K parts per tile (0: no split-K)
+    int32_t k_rotate;    // 1: whole tiles start their k loop at their own
+                         // offset (see unit_kblock)
+    int32_t l2_prefetch; // k-blocks of B to prefetch into L2 ahead of the ring (0: off)
     int64_t sk_q;        // Stream-K iterations per CTA (floor)
     int64_t sk_r;        // CTAs [0, sk_r) take sk_q + 1
 };
@@ -49,6 +62,8 @@ struct Unit {
     int32_t role;
     int32_t npeers;  // OWNER only
     int32_t tm, tn;  // tile row / column
+    int32_t slot;    // PEER: its partial-tile slot; OWNER: slot of its first
+                     // peer (the peers' slots follow in ascending k)
 };
 
 struct Cursor {
@@ -57,6 +72,21 @@ struct Cursor {
 };
 
 PSM_HD int64_t imin64(int64_t a, int64_t b) { return a < b ? a : b; }
+
+// k-block visited at step i of a unit.  Partial units walk [k0, k1) in order.
+// With k_rotate, a whole tile t starts at block floor(t * ipt / tiles) and
+// wraps around: when one row of tiles streams a B that is read exactly once,
+// the tiles then read different rows of B at any moment instead of all
+// crowding the same few, which spreads the reads over the DRAM channels.
+// Only the fp32 summation order of such a tile changes.
+PSM_HD int32_t unit_kblock(const Sched& s, int32_t tile, int32_t k0, int32_t k1, int32_t i) {
+    if (s.k_rotate && k0 == 0 && k1 == s.ipt) {
+        const int32_t rot = (int32_t)(((int64_t)tile * s.ipt) / (s.tiles > 0 ? s.tiles : 1));
+        const int32_t kb = i + rot;
+        return kb >= s.ipt ? kb - s.ipt : kb;
+    }
+    return k0 + i;
+}
 
 PSM_HD void tile_coords(const Sched& s, int32_t t, int32_t& tm, int32_t& tn) {
     if (s.group_m > 0) {
@@ -91,7 +121,7 @@ PSM_HD void cursor_init(const Sched& s, int32_t cta, Cursor& c) {
     } else {
         c.it = c.it_end = 0;
     }
-    c.next_whole = s.sk_tiles + cta;
+    c.next_whole = s.sk_tiles + cta;  // split-K: the unit counter
 }
 
 PSM_HD bool cursor_next(const Sched& s, int32_t cta, Cursor& c, Unit& u) {
@@ -104,6 +134,7 @@ PSM_HD bool cursor_next(const Sched& s, int32_t cta, Cursor& c, Unit& u) {
         u.k0 = (int32_t)k0;
         u.k1 = (int32_t)(end - tile_first);
         c.it = end;
+        u.slot = cta;
         if (u.k0 > 0) {
             u.role = ROLE_PEER;
             u.npeers = 0;
@@ -113,6 +144,33 @@ PSM_HD bool cursor_next(const Sched& s, int32_t cta, Cursor& c, Unit& u) {
         } else {
             u.role = ROLE_OWNER;
             u.npeers = (int32_t)(sk_cta_of(s, tile_first + s.ipt - 1) - cta);
+            u.slot = cta + 1;
+        }
+        tile_coords(s, u.tile, u.tm, u.tn);
+        return true;
+    }
+    if (s.split > 0) {
+        const int64_t total = (int64_t)s.tiles * s.split;
+        if (c.next_whole >= total) return false;
+        const int64_t uid = c.next_whole;
+        c.next_whole += s.grid;
+        const int32_t part = s.split - 1 - (int32_t)(uid / s.tiles);
+        u.tile = (int32_t)(uid % s.tiles);
+        u.k0 = (int32_t)(((int64_t)part * s.ipt) / s.split);
+        u.k1 = (int32_t)(((int64_t)(part + 1) * s.ipt) / s.split);
+        const int32_t first_peer_slot = u.tile * (s.split - 1);
+        if (s.split == 1) {
+            u.role = ROLE_FULL;
+            u.npeers = 0;
+            u.slot = 0;
+        } else if (part == 0) {
+            u.role = ROLE_OWNER;
+            u.npeers = s.split - 1;
+            u.slot = first_peer_slot;
+        } else {
+            u.role = ROLE_PEER;
+            u.npeers = 0;
+            u.slot = first_peer_slot + part - 1;
         }
         tile_coords(s, u.tile, u.tm, u.tn);
         return true;
@@ -123,6 +181,7 @@ PSM_HD bool cursor_next(const Sched& s, int32_t cta, Cursor& c, Unit& u) {
         u.k1 = s.ipt;
         u.role = ROLE_FULL;
         u.npeers = 0;
+        u.slot = 0;
         tile_coords(s, u.tile, u.tm, u.tn);
         c.next_whole = s.persistent ? c.next_whole + s.grid : s.tiles;
         return true;

@@ -71,8 +71,7 @@ SHAPES = [
 
 @pytest.mark.parametrize("M,N,K", SHAPES)
 @pytest.mark.parametrize("sms", [148, 152])
-@pytest.mark.parametrize("tile_n", [128, 256])
-@pytest.mark.parametrize("cm", [1, 2])
+@pytest.mark.parametrize("tile_n,cm", [(64, 1), (128, 1), (128, 2), (256, 1), (256, 2)])
 def test_streamk_units_match_oracle(lib, M, N, K, sms, tile_n, cm):
     for g, two in ((sms, 1), (8, 1), (sms, 0), (2, 1)):
         p = B.Plan(M, N, K, B.GEMM_BF16, 0, 1, "streamk", offline_sms=sms, tile_n=tile_n,
@@ -103,6 +102,66 @@ def test_streamk_units_match_oracle(lib, M, N, K, sms, tile_n, cm):
         else:
             assert ws == 0
         p.close()
+
+
+@pytest.mark.parametrize("M,N,K", SHAPES)
+@pytest.mark.parametrize("cm", [1, 2])
+def test_all_streamk_mode_matches_oracle(lib, M, N, K, cm):
+    g = 152
+    p = B.Plan(M, N, K, B.GEMM_F16, 0, 0, "streamk", offline_sms=g, cluster_m=cm, sk_mode=1)
+    o = Schedule(M, N, K, 128 * cm, p.info("tile_n"), 64, g // cm, all_streamk=True)
+    assert p.info("sk_tiles") == o.tiles == o.sk_tiles and o.dp_tiles == 0
+    sk_units = _roles_from_oracle(o)
+    for c in range(p.info("grid")):
+        assert p.units(c) == sk_units[c // cm]
+    p.close()
+
+
+@pytest.mark.parametrize("M,N,K", SHAPES)
+@pytest.mark.parametrize("cm", [1, 2])
+def test_splitk_units(lib, M, N, K, cm):
+    from oracle.streamk_schedule import splitk_parts
+    for S in (0, 1, 2, 3, 5):
+        p = B.Plan(M, N, K, B.GEMM_BF16, 0, 1, "splitk", offline_sms=152, cluster_m=cm, split_k=S)
+        tiles, ipt, S_got = p.info("tiles"), p.info("iters_per_tile"), p.info("split_k")
+        if S:
+            assert S_got == min(S, ipt)
+        assert 1 <= S_got <= max(1, ipt)
+        parts = splitk_parts(ipt, S_got)
+        seen = {}
+        for c in range(p.info("grid")):
+            units = p.units(c)
+            roles = [u[3] for u in units]
+            # a CTA runs all its peer units before any owner unit
+            if B.ROLE_OWNER in roles:
+                assert B.ROLE_PEER not in roles[roles.index(B.ROLE_OWNER):]
+            for tile, k0, k1, role, npeers in units:
+                part = parts.index((k0, k1))
+                key = (tile, part)
+                if c % cm == 1:
+                    assert seen[key] == c - 1      # the pair's second CTA repeats the unit
+                    continue
+                assert key not in seen
+                seen[key] = c
+                if S_got == 1:
+                    assert role == B.ROLE_FULL
+                elif part == 0:
+                    assert role == B.ROLE_OWNER and npeers == S_got - 1
+                else:
+                    assert role == B.ROLE_PEER and npeers == 0
+        assert len(seen) == tiles * S_got
+        ws = p.workspace_size
+        assert (ws == 0) == (S_got == 1)
+        p.close()
+
+
+def test_half_height_a_for_short_m(lib):
+    p = B.Plan(64, 8192, 8192, B.GEMM_F16, 0, 0, "streamk", offline_sms=148, tile_n=128)
+    assert p.info("a_rows_per_stage") == 64 and p.info("stages") == 8
+    p.close()
+    p = B.Plan(65, 8192, 8192, B.GEMM_F16, 0, 0, "streamk", offline_sms=148, tile_n=128)
+    assert p.info("a_rows_per_stage") == 128 and p.info("stages") == 6
+    p.close()
 
 
 @pytest.mark.parametrize("M,N,K", SHAPES)
@@ -147,7 +206,18 @@ def test_default_options(lib):
     p.close()
     p = B.Plan(64, 8192, 8192, B.GEMM_F16, 0, 0, "dp", offline_sms=148)
     assert p.info("tile_n") == 128 and p.info("group_m") == 0 and p.info("tiles") == 64
+    assert p.info("a_rows_per_stage") == 64 and p.info("stages") == 8
+    assert p.info("l2_prefetch") == 0 and p.info("k_rotate") == 0
     p.close()
+    p = B.Plan(512, 512, 512, B.GEMM_F16, 0, 0, "dp", offline_sms=148)
+    assert p.info("tile_n") == 64 and p.info("tiles") == 32 and p.info("stages") == 8
+    p.close()
+    p = B.Plan(2304, 2304, 8192, B.GEMM_BF16, 0, 1, "streamk", offline_sms=152)
+    assert p.info("tile_n") == 256 and p.info("cluster_m") == 2 and p.info("tiles") == 81
+    p.close()
+    with pytest.raises(B.GemmError) as e:
+        B.Plan(512, 512, 512, B.GEMM_F16, 0, 0, "dp", offline_sms=148, tile_n=64, cluster_m=2)
+    assert e.value.status == B.GEMM_ERR_UNSUPPORTED
 
 
 def test_argument_errors(lib):
@@ -161,7 +231,7 @@ def test_argument_errors(lib):
         B.gemm_plan_create_offline(8, 8, 8, 0, 0, 0, 0, 0)
     assert e.value.status == B.GEMM_ERR_INVALID_ARG
     p = B.Plan(256, 256, 256, B.GEMM_F16, 0, 0, "streamk", offline_sms=148)
-    for key, val, st in ((B.GEMM_OPT_TILE_N, 64, B.GEMM_ERR_UNSUPPORTED),
+    for key, val, st in ((B.GEMM_OPT_TILE_N, 96, B.GEMM_ERR_UNSUPPORTED),
                          (B.GEMM_OPT_GRID, 149, B.GEMM_ERR_UNSUPPORTED),
                          (B.GEMM_OPT_TWO_TILES, 2, B.GEMM_ERR_UNSUPPORTED),
                          (99, 0, B.GEMM_ERR_INVALID_ARG)):

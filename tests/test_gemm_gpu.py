@@ -13,7 +13,7 @@ from tests.gpu_util import Workspace, ensure_built, run, to_device
 
 pytestmark = pytest.mark.gpu
 
-SCHEDS = ["dp", "persistent", "streamk"]
+SCHEDS = ["dp", "persistent", "streamk", "splitk"]
 LAYOUTS = [(0, 0), (0, 1), (1, 0), (1, 1)]
 
 
@@ -51,8 +51,8 @@ def test_parity_small(sched, dtype, la, lb):
         if la == 1 and M % 8:
             continue
         A, Bm, dA, dB = _case(M, N, K, dtype, la, lb, ("normal", 1.0), 10 + i)
-        for tile_n in (128, 256):
-            for cm in (1, 2):
+        for tile_n in (64, 128, 256):
+            for cm in ((1,) if tile_n == 64 else (1, 2)):
                 p = B.Plan(M, N, K, dtype, la, lb, sched, tile_n=tile_n, cluster_m=cm)
                 Cb = run(p, dA, dB, M, N, ws)
                 _check_full(Cb, A, Bm, M, N, K, dtype, la, lb)
@@ -83,8 +83,8 @@ def test_streamk_forced_grids_integer(dtype):
     _, _, Cref = oracle.gemm(A, Bm, M, N, K, dtype, 0, 0)
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     ws = Workspace()
-    for tile_n in (128, 256):
-        for cm in (1, 2):
+    for tile_n in (64, 128, 256):
+        for cm in ((1,) if tile_n == 64 else (1, 2)):
             tiles = -(-3 // cm) * (N // tile_n)
             for g in sorted({2, 8, 14, tiles * cm, sms}):
                 for two in (0, 1):
@@ -93,6 +93,62 @@ def test_streamk_forced_grids_integer(dtype):
                     Cb = run(p, dA, dB, M, N, ws)
                     assert np.array_equal(Cb, Cref), (tile_n, cm, g, two)
                     p.close()
+
+
+@pytest.mark.parametrize("dtype", [inputs.F16, inputs.BF16])
+def test_all_streamk_mode_and_short_m(dtype):
+    ws = Workspace()
+    for (M, N, K), la, lb in (((384, 1024, 2048), 0, 1), ((64, 2048, 3000 // 8 * 8), 0, 0),
+                              ((40, 520, 1032), 0, 1), ((64, 1024, 1024), 1, 0)):
+        A, Bm, dA, dB = _case(M, N, K, dtype, la, lb, inputs.INT_LAW, 15)
+        _, _, Cref = oracle.gemm(A, Bm, M, N, K, dtype, la, lb)
+        for cm in (1, 2):
+            for mode in (0, 1):
+                p = B.Plan(M, N, K, dtype, la, lb, "streamk", cluster_m=cm, sk_mode=mode)
+                if M <= 64 and cm == 1 and p.info("tile_n") == 128:
+                    assert p.info("a_rows_per_stage") == 64
+                first = run(p, dA, dB, M, N, ws)
+                assert np.array_equal(first, Cref), (M, N, K, cm, mode)
+                assert np.array_equal(run(p, dA, dB, M, N, ws), first)
+                p.close()
+
+
+@pytest.mark.parametrize("dtype", [inputs.F16, inputs.BF16])
+def test_splitk_parts_integer_exact(dtype):
+    ws = Workspace()
+    for (M, N, K), la, lb in (((384, 1024, 2048), 0, 1), ((64, 2048, 3000 // 8 * 8), 0, 0),
+                              ((300, 264, 1000), 1 if 300 % 8 == 0 else 0, 0)):
+        A, Bm, dA, dB = _case(M, N, K, dtype, la, lb, inputs.INT_LAW, 16)
+        _, _, Cref = oracle.gemm(A, Bm, M, N, K, dtype, la, lb)
+        for cm in (1, 2):
+            for S in (0, 2, 3, 7):
+                p = B.Plan(M, N, K, dtype, la, lb, "splitk", cluster_m=cm, split_k=S)
+                first = run(p, dA, dB, M, N, ws)
+                assert np.array_equal(first, Cref), (M, N, K, cm, S)
+                assert np.array_equal(run(p, dA, dB, M, N, ws), first)
+                p.close()
+
+
+@pytest.mark.parametrize("sched", SCHEDS)
+def test_k_rotation_and_l2_prefetch(sched):
+    # whole tiles visiting their k-blocks in rotated order, and B prefetched
+    # into L2 ahead of the ring: same bits on integers, within the bound on
+    # real values, deterministic
+    ws = Workspace()
+    for (M, N, K, dtype, la, lb) in ((64, 1024, 2048, inputs.F16, 0, 0),
+                                     (300, 520, 1000, inputs.BF16, 0, 1),
+                                     (256, 512, 4096, inputs.BF16, 1, 1)):
+        for law in (inputs.INT_LAW, ("normal", 1.0)):
+            A, Bm, dA, dB = _case(M, N, K, dtype, la, lb, law, 17)
+            for tile_n, cm, rot, pf in ((64, 1, 1, 0), (128, 1, 1, 8), (128, 2, 0, 16),
+                                        (256, 2, 1, 4)):
+                p = B.Plan(M, N, K, dtype, la, lb, sched, tile_n=tile_n, cluster_m=cm,
+                           k_rotate=rot, l2_prefetch=pf)
+                assert p.info("k_rotate") == rot and p.info("l2_prefetch") == pf
+                Cb = run(p, dA, dB, M, N, ws)
+                _check_full(Cb, A, Bm, M, N, K, dtype, la, lb, exact=law == inputs.INT_LAW)
+                assert np.array_equal(run(p, dA, dB, M, N, ws), Cb)
+                p.close()
 
 
 def test_streamk_deterministic_and_within_bound():

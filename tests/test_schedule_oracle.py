@@ -92,6 +92,10 @@ def test_coverage_exhaustive_small():
                     for two in (True, False):
                         s = Schedule(tiles_m * 16, tiles_n * 16, ipt * 8, 16, 16, 8, g, two)
                         _check_cover(s)
+                    s = Schedule(tiles_m * 16, tiles_n * 16, ipt * 8, 16, 16, 8, g,
+                                 all_streamk=True)
+                    assert s.sk_tiles == s.tiles and s.dp_tiles == 0
+                    _check_cover(s)
 
 
 def test_coverage_workloads():

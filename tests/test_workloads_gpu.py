@@ -15,7 +15,7 @@ from tests.gpu_util import Workspace, ensure_built, run, to_device
 
 pytestmark = pytest.mark.gpu
 
-SCHEDS = ["dp", "persistent", "streamk"]
+SCHEDS = ["dp", "persistent", "streamk", "splitk"]
 FULL_COMPARE = {"square512_f16", "skinny64x8192x8192_f16"}
 
 
@@ -64,5 +64,5 @@ def test_workload(name, integer):
         outs[sched] = Cb
         p.close()
     if integer:
-        assert np.array_equal(outs["dp"], outs["streamk"])
-        assert np.array_equal(outs["dp"], outs["persistent"])
+        for sched in SCHEDS[1:]:
+            assert np.array_equal(outs["dp"], outs[sched])
