@@ -125,7 +125,12 @@ enum {
     GEMM_OPT_K_ROTATE = 10,
     /* k-blocks of B prefetched into L2 ahead of the shared-memory ring
      * (0 = off, the default; up to 256). */
-    GEMM_OPT_L2_PREFETCH = 11
+    GEMM_OPT_L2_PREFETCH = 11,
+    /* with 2-CTA clusters: 1 = one tcgen05 pair MMA (cta_group::2, 256 x BN)
+     * per k-step issued for both CTAs, each CTA holding only its half of B
+     * (deeper ring); 0 (default) = each CTA runs its own 128 x BN MMA on a
+     * full B tile assembled by multicast. */
+    GEMM_OPT_PAIR_MMA = 12
 };
 
 /* Keys for gemm_plan_get_info. */
@@ -146,7 +151,8 @@ enum {
     GEMM_INFO_A_ROWS_PER_STAGE = 17,/* rows of A each ring stage loads: 128, or 64 when M <= 64 */
     GEMM_INFO_SPLIT_K = 18,         /* split-K parts per tile (0 unless GEMM_SCHED_SPLITK) */
     GEMM_INFO_K_ROTATE = 19,        /* 1 when whole tiles rotate their k order */
-    GEMM_INFO_L2_PREFETCH = 20      /* k-blocks of B prefetched into L2 ahead of the ring */
+    GEMM_INFO_L2_PREFETCH = 20,     /* k-blocks of B prefetched into L2 ahead of the ring */
+    GEMM_INFO_PAIR_MMA = 21         /* 1 when the cluster runs pair MMAs */
 };
 
 /* Roles of a work unit reported by gemm_plan_units. */

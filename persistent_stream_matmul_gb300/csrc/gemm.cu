@@ -57,11 +57,11 @@ struct gemm_plan {
     int device, num_sms, offline;
     // options
     int opt_grid, opt_group_m, opt_tile_n, opt_two_tiles, inject_skip, opt_cluster_m, opt_sk_mode;
-    int opt_split, opt_k_rotate, opt_l2_prefetch;
+    int opt_split, opt_k_rotate, opt_l2_prefetch, opt_pair_mma;
     int64_t wait_limit_us;
     int max_pair_ctas;  // CTAs co-resident as 2-CTA clusters (0: unknown)
     // derived
-    int BN, CM, AROWS, ctas, stages, smem_bytes;
+    int BN, CM, AROWS, PAIR, ctas, stages, smem_bytes;
     Sched s;
     size_t ws_flag_bytes, ws_bytes;
     // device state
@@ -72,7 +72,7 @@ struct gemm_plan {
     bool tm_valid;
     CUtensorMap tmA, tmB;
     const void* flags_cleared_for;
-    bool attr_set[16];
+    bool attr_set[20];
     unsigned long long* trace;  // optional per-CTA stamps (caller-owned device buffer)
     size_t trace_bytes;
 };
@@ -84,9 +84,9 @@ bool valid_enums(int dtype, int la, int lb, int sched) {
            (lb == 0 || lb == 1) && (sched >= 0 && sched <= 3);
 }
 
-template <int BN, bool BF, int CM, int AROWS = 128>
+template <int BN, bool BF, int CM, int AROWS = 128, bool PAIR_MMA = false>
 void* kernel_ptr() {
-    return reinterpret_cast<void*>(&gemm_kernel<BN, BF, CM, AROWS>);
+    return reinterpret_cast<void*>(&gemm_kernel<BN, BF, CM, AROWS, PAIR_MMA>);
 }
 
 template <int CM>
@@ -96,8 +96,12 @@ void* pick_kernel_cm(int BN, int dtype) {
     return dtype == GEMM_BF16 ? kernel_ptr<128, true, CM>() : kernel_ptr<128, false, CM>();
 }
 
-void* pick_kernel(int BN, int dtype, int CM, int AROWS = 128) {
+void* pick_kernel(int BN, int dtype, int CM, int AROWS = 128, int PAIR = 0) {
     const bool bf = dtype == GEMM_BF16;
+    if (PAIR) {  // CM = 2, BN = 128 or 256
+        if (BN == 256) return bf ? kernel_ptr<256, true, 2, 128, true>() : kernel_ptr<256, false, 2, 128, true>();
+        return bf ? kernel_ptr<128, true, 2, 128, true>() : kernel_ptr<128, false, 2, 128, true>();
+    }
     if (BN == 64) {  // only with CM = 1
         if (AROWS == 64) return bf ? kernel_ptr<64, true, 1, 64>() : kernel_ptr<64, false, 1, 64>();
         return bf ? kernel_ptr<64, true, 1>() : kernel_ptr<64, false, 1>();
@@ -107,19 +111,22 @@ void* pick_kernel(int BN, int dtype, int CM, int AROWS = 128) {
     return CM == 2 ? pick_kernel_cm<2>(BN, dtype) : pick_kernel_cm<1>(BN, dtype);
 }
 
-int kernel_index(int BN, int dtype, int CM, int AROWS) {
+int kernel_index(int BN, int dtype, int CM, int AROWS, int PAIR) {
     const int bf = dtype == GEMM_BF16 ? 1 : 0;
+    if (PAIR) return 14 + 2 * (BN == 256 ? 1 : 0) + bf;
     if (BN == 64) return 10 + 2 * (AROWS == 64 ? 1 : 0) + bf;
     if (AROWS == 64) return 8 + bf;
     return (BN == 256 ? 4 : 0) + 2 * bf + (CM == 2 ? 1 : 0);
 }
 
-int smem_for(int BN, int AROWS = 128) {
+int smem_for(int BN, int AROWS = 128, int PAIR = 0) {
+    if (PAIR) return BN == 256 ? Cfg<256, 128, true>::SMEM_BYTES : Cfg<128, 128, true>::SMEM_BYTES;
     if (BN == 64) return AROWS == 64 ? Cfg<64, 64>::SMEM_BYTES : Cfg<64>::SMEM_BYTES;
     if (AROWS == 64) return Cfg<128, 64>::SMEM_BYTES;
     return BN == 256 ? Cfg<256>::SMEM_BYTES : Cfg<128>::SMEM_BYTES;
 }
-int stages_for(int BN, int AROWS = 128) {
+int stages_for(int BN, int AROWS = 128, int PAIR = 0) {
+    if (PAIR) return BN == 256 ? Cfg<256, 128, true>::STAGES : Cfg<128, 128, true>::STAGES;
     if (BN == 64) return AROWS == 64 ? Cfg<64, 64>::STAGES : Cfg<64>::STAGES;
     if (AROWS == 64) return Cfg<128, 64>::STAGES;
     return BN == 256 ? Cfg<256>::STAGES : Cfg<128>::STAGES;
@@ -209,9 +216,12 @@ gemm_status_t derive(gemm_plan* p) {
     p->CM = CM;
     // one row of tiles with at most 64 valid rows: load only those rows of A
     p->AROWS = (p->M <= 64 && CM == 1 && BN <= 128) ? 64 : 128;
+    // pair MMA (tcgen05 cta_group::2) for 2-CTA clusters: each CTA keeps
+    // only its half of B, so the ring is deeper
+    p->PAIR = (CM == 2 && p->opt_pair_mma == 1) ? 1 : 0;
     p->ctas = s.grid * CM;
-    p->stages = stages_for(BN, p->AROWS);
-    p->smem_bytes = smem_for(BN, p->AROWS);
+    p->stages = stages_for(BN, p->AROWS, p->PAIR);
+    p->smem_bytes = smem_for(BN, p->AROWS, p->PAIR);
     if (p->schedule == GEMM_SCHED_STREAMK && s.sk_tiles > 0) {
         p->ws_flag_bytes = ((size_t)s.sk_tiles * CM * 8 + 255) / 256 * 256;
         p->ws_bytes = p->ws_flag_bytes + (size_t)p->ctas * BM * BN * sizeof(float);
@@ -286,6 +296,7 @@ gemm_status_t make_plan(gemm_plan_t* out, int64_t M, int64_t N, int64_t K, int d
     p->opt_split = 0;
     p->opt_k_rotate = 0;
     p->opt_l2_prefetch = -1;
+    p->opt_pair_mma = 0;
     p->wait_limit_us = 1000000;
     if (offline) {
         if (num_sms <= 0) { delete p; return GEMM_ERR_INVALID_ARG; }
@@ -466,6 +477,10 @@ gemm_status_t gemm_plan_set_option(gemm_plan_t p, int key, int64_t value) {
             if (value < 0 || value > 256) return GEMM_ERR_UNSUPPORTED;
             p->opt_l2_prefetch = (int)value;
             break;
+        case GEMM_OPT_PAIR_MMA:
+            if (value != 0 && value != 1) return GEMM_ERR_UNSUPPORTED;
+            p->opt_pair_mma = (int)value;
+            break;
         default:
             return GEMM_ERR_INVALID_ARG;
     }
@@ -498,6 +513,7 @@ gemm_status_t gemm_plan_get_info(gemm_plan_t p, int key, int64_t* value) {
         case GEMM_INFO_SPLIT_K: v = p->s.split; break;
         case GEMM_INFO_K_ROTATE: v = p->s.k_rotate; break;
         case GEMM_INFO_L2_PREFETCH: v = p->s.l2_prefetch; break;
+        case GEMM_INFO_PAIR_MMA: v = p->PAIR; break;
         default: return GEMM_ERR_INVALID_ARG;
     }
     *value = v;
@@ -533,8 +549,8 @@ gemm_status_t gemm_run(gemm_plan_t p, const void* A, const void* B, void* C, voi
     gemm_status_t es = encode_maps(p, A, B);
     if (es != GEMM_OK) return es;
 
-    void* fn = pick_kernel(p->BN, p->dtype, p->CM, p->AROWS);
-    const int bi = kernel_index(p->BN, p->dtype, p->CM, p->AROWS);
+    void* fn = pick_kernel(p->BN, p->dtype, p->CM, p->AROWS, p->PAIR);
+    const int bi = kernel_index(p->BN, p->dtype, p->CM, p->AROWS, p->PAIR);
     if (!p->attr_set[bi]) {
         if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, p->smem_bytes) !=
             cudaSuccess)
@@ -558,7 +574,7 @@ gemm_status_t gemm_run(gemm_plan_t p, const void* A, const void* B, void* C, voi
                       : nullptr;
     kp.status = p->d_status;
     kp.idesc = idesc_f16(p->dtype == GEMM_BF16, p->layout_a == GEMM_COL_MAJOR,
-                         p->layout_b == GEMM_ROW_MAJOR, BM, p->BN);
+                         p->layout_b == GEMM_ROW_MAJOR, p->PAIR ? 2 * BM : BM, p->BN);
     kp.epoch = next_epoch();
     kp.a_mn = p->layout_a == GEMM_COL_MAJOR;
     kp.b_mn = p->layout_b == GEMM_ROW_MAJOR;

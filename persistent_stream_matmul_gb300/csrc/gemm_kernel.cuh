@@ -62,16 +62,22 @@ enum : uint32_t { BAR_EPI_SYNC = 1, BAR_EPI_VOTE = 2 };  // named barriers (0 = 
 // stage's B tile, so those accumulator rows hold garbage that is never stored
 // (each output row depends only on its own row of A); the smaller stage lets
 // the ring hold more B in flight.
-template <int BN, int AROWS = 128>
+template <int BN, int AROWS = 128, bool PAIR_MMA = false>
 struct Cfg {
     static constexpr int A_STAGE_BYTES = AROWS * BK * 2;
-    static constexpr int B_STAGE_BYTES = BN * BK * 2;
+    // a pair MMA keeps only this CTA's half of the B tile in its ring
+    static constexpr int B_STAGE_BYTES = (PAIR_MMA ? BN / 2 : BN) * BK * 2;
     static constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
     static constexpr int STAGES_FIT = (192 * 1024) / STAGE_BYTES;  // 4, 6, 8 or 12
     static constexpr int STAGES = STAGES_FIT > 12 ? 12 : STAGES_FIT;
     static constexpr int TMEM_COLS = 2 * BN;  // two accumulators; 256 or 512
     static constexpr int BAR_BYTES = 256;
-    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + BAR_BYTES + 1024;
+    // A pair MMA reads half tiles through descriptors of full-tile shape: 32 KB
+    // of slack after the ring keeps any read past a half inside this CTA's
+    // shared memory.
+    static constexpr int SLACK_BYTES = PAIR_MMA ? 32 * 1024 : 0;
+    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + SLACK_BYTES + BAR_BYTES + 1024;
+    static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
     static_assert(BN == 64 || BN == 128 || BN == 256, "tile width");
     static_assert(AROWS == 128 || AROWS == 64, "rows of A per stage");
     static_assert(AROWS == 128 || A_STAGE_BYTES + B_STAGE_BYTES >= BM * BK * 2,
@@ -157,24 +163,25 @@ __device__ __forceinline__ uint32_t pack2(float a, float b) {
     }
 }
 
-template <int BN, bool OUT_BF16, int CM, int AROWS = 128>
+template <int BN, bool OUT_BF16, int CM, int AROWS = 128, bool PAIR_MMA = false>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ KParams p) {
-    using Cf = Cfg<BN, AROWS>;
+    using Cf = Cfg<BN, AROWS, PAIR_MMA>;
+    static_assert(!PAIR_MMA || CM == 2, "a pair MMA needs a 2-CTA cluster");
     static_assert(AROWS == 128 || CM == 1, "half-height A only without clusters");
     static_assert(BN >= 128 || CM == 1, "64-wide tiles only without clusters");
     constexpr int STAGES = Cf::STAGES;
     static_assert(CM == 1 || CM == 2, "cluster size");
-    constexpr uint16_t PAIR = 0x3;
+    constexpr uint16_t PAIR_MASK = 0x3;
     extern __shared__ uint8_t smem_raw[];
 
     // 1024-byte aligned base: the 128-byte swizzle pattern repeats every 1 KB
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
     const uint32_t sbase = raw + pad;
-    uint8_t* bar_area = smem_raw + pad + STAGES * Cf::STAGE_BYTES;
-    const uint32_t bar_base = sbase + STAGES * Cf::STAGE_BYTES;
+    uint8_t* bar_area = smem_raw + pad + STAGES * Cf::STAGE_BYTES + Cf::SLACK_BYTES;
+    const uint32_t bar_base = sbase + STAGES * Cf::STAGE_BYTES + Cf::SLACK_BYTES;
     auto full_bar = [&](int s) { return bar_base + 8u * s; };
     auto empty_bar = [&](int s) { return bar_base + 8u * (STAGES + s); };
     auto tfull_bar = [&](int b) { return bar_base + 8u * (2 * STAGES + b); };
@@ -191,13 +198,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int rank = CM == 2 ? (int)cluster_ctarank() : 0;
 
     if (threadIdx.x == 0) {
+        // pair MMA: the first CTA's full barriers count both CTAs' copies, one
+        // multicast commit frees a stage in both CTAs, and the first CTA's
+        // accumulator-empty barriers count the epilogue warps of both
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(full_bar(s), 1);
-            mbar_init(empty_bar(s), CM);
+            mbar_init(empty_bar(s), PAIR_MMA ? 1 : CM);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(tfull_bar(b), 1);
-            mbar_init(tempty_bar(b), EPI_THREADS / 32);
+            mbar_init(tempty_bar(b), (PAIR_MMA ? 2 : 1) * EPI_THREADS / 32);
         }
         mbar_init(done_bar, 1);
         *abort_flag = 0;
@@ -208,8 +218,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         tma_prefetch_desc(&tmB);
     }
     if (warp == 1) {
-        tmem_alloc(smem_addr(tmem_slot), Cf::TMEM_COLS);
-        tmem_relinquish();
+        if constexpr (PAIR_MMA) {
+            tmem_alloc_pair(smem_addr(tmem_slot), Cf::TMEM_COLS);
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc(smem_addr(tmem_slot), Cf::TMEM_COLS);
+            tmem_relinquish();
+        }
     }
     tc_fence_before_sync();
     if constexpr (CM == 2) {
@@ -282,6 +297,28 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     const uint32_t sa = sbase + stage * Cf::STAGE_BYTES;
                     const uint32_t sb = sa + Cf::A_STAGE_BYTES;
                     const int k_el = kb * BK;
+                    if constexpr (PAIR_MMA) {
+                        // both CTAs' copies complete on the first CTA's barrier
+                        const uint32_t fbc = mapa_shared(fb, 0);
+                        if (rank == 0) mbar_arrive_expect_tx(fb, 2 * Cf::STAGE_BYTES);
+                        if (!p.a_mn) {
+                            tma_load_2d_pair(sa, &tmA, fbc, k_el, m0, pol_a);
+                        } else {
+#pragma unroll
+                            for (int c = 0; c < BM / 64; ++c)
+                                tma_load_2d_pair(sa + c * MN_CHUNK_BYTES, &tmA, fbc, m0 + 64 * c,
+                                                 k_el, pol_a);
+                        }
+                        const int nb = n0 + rank * (BN / 2);  // this CTA's half of B
+                        if (!p.b_mn) {
+                            tma_load_2d_pair(sb, &tmB, fbc, k_el, nb, policy);
+                        } else {
+#pragma unroll
+                            for (int c = 0; c < BN / 128; ++c)
+                                tma_load_2d_pair(sb + c * MN_CHUNK_BYTES, &tmB, fbc, nb + 64 * c,
+                                                 k_el, policy);
+                        }
+                    } else {
                     mbar_arrive_expect_tx(fb, Cf::STAGE_BYTES);
                     if (!p.a_mn) {
                         tma_load_2d(sa, &tmA, fb, k_el, m0, pol_a);  // box of AROWS rows
@@ -304,14 +341,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         if (!p.b_mn) {
                             const int half = BN / 2;  // rows of the K-major box
                             tma_load_2d_multicast(sb + rank * half * 128, &tmB, fb, k_el,
-                                                  n0 + rank * half, PAIR, policy);
+                                                  n0 + rank * half, PAIR_MASK, policy);
                         } else {
 #pragma unroll
                             for (int c = rank * (BN / 128); c < (rank + 1) * (BN / 128); ++c)
                                 tma_load_2d_multicast(sb + c * MN_CHUNK_BYTES, &tmB, fb,
-                                                      n0 + 64 * c, k_el, PAIR, policy);
+                                                      n0 + 64 * c, k_el, PAIR_MASK, policy);
                         }
                     }
+                    }  // not a pair MMA
                     filled |= 1u << stage;
                     fill_parity = (fill_parity & ~(1u << stage)) | (phase << stage);
                     if (++stage == STAGES) {
@@ -326,13 +364,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             // has released it
             for (int s = 0; s < STAGES; ++s)
                 if (filled & (1u << s)) {
-                    mbar_wait(full_bar(s), (fill_parity >> s) & 1u, p.pipe_limit_ns);
+                    // (pair MMA: the second CTA's copies complete on the first
+                    // CTA's barrier, so it waits for the stage's release alone)
+                    if (!PAIR_MMA || rank == 0)
+                        mbar_wait(full_bar(s), (fill_parity >> s) & 1u, p.pipe_limit_ns);
                     mbar_wait(empty_bar(s), (fill_parity >> s) & 1u, p.pipe_limit_ns);
                 }
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
+        // (pair MMA: the first CTA of the pair issues for both)
+        if (lane == 0 && (!PAIR_MMA || rank == 0)) {
             Cursor cur;
             cursor_init(p.s, unit_cta, cur);
             Unit u;
@@ -367,10 +409,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         const uint64_t bdesc =
                             p.b_mn ? smem_desc_sw128(sb + kk * 16 * 128, MN_CHUNK_BYTES, SW_ATOM_BYTES)
                                    : smem_desc_sw128(sb + kk * UMMA_K * 2, 16, SW_ATOM_BYTES);
-                        mma_f16_ss(d_tmem, adesc, bdesc, p.idesc, (i > 0 || kk > 0) ? 1u : 0u);
+                        if constexpr (PAIR_MMA)
+                            mma_f16_ss_pair(d_tmem, adesc, bdesc, p.idesc, (i > 0 || kk > 0) ? 1u : 0u);
+                        else
+                            mma_f16_ss(d_tmem, adesc, bdesc, p.idesc, (i > 0 || kk > 0) ? 1u : 0u);
                     }
-                    if constexpr (CM == 2) {
-                        mma_commit_multicast(empty_bar(stage), PAIR);  // both halves of B were read
+                    if constexpr (PAIR_MMA) {
+                        mma_commit_pair_multicast(empty_bar(stage), PAIR_MASK);  // frees both rings
+                    } else if constexpr (CM == 2) {
+                        mma_commit_multicast(empty_bar(stage), PAIR_MASK);  // both halves of B were read
                     } else {
                         mma_commit(empty_bar(stage));
                     }
@@ -380,11 +427,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     }
                 }
                 if (!ok) break;
-                mma_commit(tfull_bar(buf));
+                if constexpr (PAIR_MMA)
+                    mma_commit_pair_multicast(tfull_bar(buf), PAIR_MASK);  // both halves of D ready
+                else
+                    mma_commit(tfull_bar(buf));
                 ++iter;
             }
             // all MMAs this thread issued are complete before TMEM is freed
-            mma_commit(done_bar);
+            if constexpr (PAIR_MMA)
+                mma_commit_pair_multicast(done_bar, 0x1);
+            else
+                mma_commit(done_bar);
             mbar_wait(done_bar, 0, p.pipe_limit_ns);
         }
     } else {
@@ -431,7 +484,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
                 tc_fence_before_sync();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(tempty_bar(buf));
+                if (lane == 0) {
+                    if constexpr (PAIR_MMA)
+                        mbar_arrive_cluster(mapa_shared(tempty_bar(buf), 0));
+                    else
+                        mbar_arrive(tempty_bar(buf));
+                }
                 __threadfence();
                 named_bar_sync(BAR_EPI_SYNC, EPI_THREADS);
                 if (et == 0 && cta != p.inject_skip_cta) post_flag(p.flags + u.tile * CM + rank, p.epoch);
@@ -502,7 +560,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
                 tc_fence_before_sync();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(tempty_bar(buf));
+                if (lane == 0) {
+                    if constexpr (PAIR_MMA)
+                        mbar_arrive_cluster(mapa_shared(tempty_bar(buf), 0));
+                    else
+                        mbar_arrive(tempty_bar(buf));
+                }
             }
             ++iter;
         }
@@ -519,7 +582,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (warp == 1) {
         __syncwarp();
         tc_fence_after_sync();
-        tmem_dealloc(tmem_base, Cf::TMEM_COLS);
+        if constexpr (PAIR_MMA)
+            tmem_dealloc_pair(tmem_base, Cf::TMEM_COLS);
+        else
+            tmem_dealloc(tmem_base, Cf::TMEM_COLS);
     }
 }
 

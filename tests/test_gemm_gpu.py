@@ -95,6 +95,29 @@ def test_streamk_forced_grids_integer(dtype):
                     p.close()
 
 
+@pytest.mark.parametrize("tile_n", [128, 256])
+@pytest.mark.parametrize("sched", SCHEDS)
+def test_pair_mma(tile_n, sched):
+    # 2-CTA clusters issuing one tcgen05 pair MMA (256 x BN) per k-step
+    ws = Workspace()
+    for i, (M, N, K) in enumerate(((256, 256, 512), (300, 264, 200), (512, 640, 1032),
+                                   (1000, 1040, 2048))):
+        for dtype in (inputs.F16, inputs.BF16):
+            for la, lb in LAYOUTS:
+                if la == 1 and M % 8:
+                    continue
+                for law in (inputs.INT_LAW, ("normal", 1.0)):
+                    A, Bm, dA, dB = _case(M, N, K, dtype, la, lb, law, 60 + i)
+                    p = B.Plan(M, N, K, dtype, la, lb, sched, tile_n=tile_n, cluster_m=2,
+                               pair_mma=1)
+                    assert p.info("pair_mma") == 1 and p.info("tile_m") == 256
+                    Cb = run(p, dA, dB, M, N, ws)
+                    _check_full(Cb, A, Bm, M, N, K, dtype, la, lb,
+                                exact=law == inputs.INT_LAW)
+                    assert np.array_equal(run(p, dA, dB, M, N, ws), Cb)
+                    p.close()
+
+
 @pytest.mark.parametrize("dtype", [inputs.F16, inputs.BF16])
 def test_all_streamk_mode_and_short_m(dtype):
     ws = Workspace()
