@@ -36,12 +36,12 @@ from persistent_stream_matmul_gb300 import inputs  # noqa: E402
 
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_BYTES = 129e6
-SCHED_NAMES = ["dp", "persistent", "streamk", "streamk_all", "splitk"]
+SCHED_NAMES = ["dp", "persistent", "streamk", "streamk_all", "splitk", "auto"]
 # name -> (schedule, options): "streamk" is the hybrid rule of the issue's final
 # version; "streamk_all" puts every tile in the Stream-K wave
 SCHED_DEFS = {"dp": ("dp", {}), "persistent": ("persistent", {}),
               "streamk": ("streamk", {}), "streamk_all": ("streamk", {"sk_mode": 1}),
-              "splitk": ("splitk", {})}
+              "splitk": ("splitk", {}), "auto": ("auto", {})}
 
 
 def peaks():

@@ -24,6 +24,13 @@
  *                             tile's K range is cut into S near-equal parts
  *                             (GEMM_OPT_SPLIT_K), computed by a persistent
  *                             grid and fixed up like Stream-K.
+ *   GEMM_SCHED_AUTO           the plan picks one of the above from the shape
+ *                             (GEMM_INFO_SCHEDULE and GEMM_INFO_SK_MODE report
+ *                             which): Stream-K for a single row of tiles;
+ *                             persistent for tiny problems, for four or more
+ *                             waves of tiles and for nearly one full wave;
+ *                             Stream-K (hybrid, or all tiles when the hybrid
+ *                             would split a few tiles many ways) otherwise.
  *
  * Conventions for every entry point:
  *  - Each call returns a gemm_status_t; nothing else crosses the ABI.  An
@@ -61,7 +68,8 @@ typedef enum {
     GEMM_SCHED_DATA_PARALLEL = 0,
     GEMM_SCHED_PERSISTENT = 1,
     GEMM_SCHED_STREAMK = 2,
-    GEMM_SCHED_SPLITK = 3
+    GEMM_SCHED_SPLITK = 3,
+    GEMM_SCHED_AUTO = 4
 } gemm_schedule_t;
 
 typedef enum {
@@ -126,10 +134,10 @@ enum {
     /* k-blocks of B prefetched into L2 ahead of the shared-memory ring
      * (0 = off, the default; up to 256). */
     GEMM_OPT_L2_PREFETCH = 11,
-    /* with 2-CTA clusters: 1 = one tcgen05 pair MMA (cta_group::2, 256 x BN)
-     * per k-step issued for both CTAs, each CTA holding only its half of B
-     * (deeper ring); 0 (default) = each CTA runs its own 128 x BN MMA on a
-     * full B tile assembled by multicast. */
+    /* with 2-CTA clusters: 1 (default) = one tcgen05 pair MMA (cta_group::2,
+     * 256 x BN) per k-step issued for both CTAs, each CTA holding only its
+     * half of B (deeper ring); 0 = each CTA runs its own 128 x BN MMA on a
+     * full B tile assembled by TMA multicast. */
     GEMM_OPT_PAIR_MMA = 12
 };
 
@@ -152,7 +160,9 @@ enum {
     GEMM_INFO_SPLIT_K = 18,         /* split-K parts per tile (0 unless GEMM_SCHED_SPLITK) */
     GEMM_INFO_K_ROTATE = 19,        /* 1 when whole tiles rotate their k order */
     GEMM_INFO_L2_PREFETCH = 20,     /* k-blocks of B prefetched into L2 ahead of the ring */
-    GEMM_INFO_PAIR_MMA = 21         /* 1 when the cluster runs pair MMAs */
+    GEMM_INFO_PAIR_MMA = 21,        /* 1 when the cluster runs pair MMAs */
+    GEMM_INFO_SCHEDULE = 22,        /* the schedule that runs (GEMM_SCHED_AUTO resolved) */
+    GEMM_INFO_SK_MODE = 23          /* 1 when every tile is in the Stream-K wave */
 };
 
 /* Roles of a work unit reported by gemm_plan_units. */

@@ -17,7 +17,8 @@ LIB_PATH = os.path.join(HERE, "libpsm_gemm.so")
 GEMM_F16, GEMM_BF16 = 0, 1
 GEMM_ROW_MAJOR, GEMM_COL_MAJOR = 0, 1
 GEMM_SCHED_DATA_PARALLEL, GEMM_SCHED_PERSISTENT, GEMM_SCHED_STREAMK, GEMM_SCHED_SPLITK = 0, 1, 2, 3
-SCHEDULES = {"dp": 0, "persistent": 1, "streamk": 2, "splitk": 3}
+GEMM_SCHED_AUTO = 4
+SCHEDULES = {"dp": 0, "persistent": 1, "streamk": 2, "splitk": 3, "auto": 4}
 
 (GEMM_OK, GEMM_ERR_INVALID_ARG, GEMM_ERR_UNSUPPORTED, GEMM_ERR_WORKSPACE, GEMM_ERR_CUDA,
  GEMM_ERR_LAUNCH, GEMM_ERR_TIMEOUT, GEMM_ERR_NO_DEVICE) = range(8)
@@ -40,7 +41,7 @@ INFO = {
     "iters_per_tile": 7, "grid": 8, "sk_tiles": 9, "sk_iters_per_cta": 10,
     "sk_iters_rem": 11, "num_sms": 12, "stages": 13, "group_m": 14, "smem_bytes": 15, "cluster_m": 16,
     "a_rows_per_stage": 17, "split_k": 18, "k_rotate": 19,
-    "l2_prefetch": 20, "pair_mma": 21,
+    "l2_prefetch": 20, "pair_mma": 21, "schedule": 22, "sk_mode": 23,
 }
 ROLE_FULL, ROLE_OWNER, ROLE_PEER = 0, 1, 2
 

@@ -58,6 +58,7 @@ struct gemm_plan {
     // options
     int opt_grid, opt_group_m, opt_tile_n, opt_two_tiles, inject_skip, opt_cluster_m, opt_sk_mode;
     int opt_split, opt_k_rotate, opt_l2_prefetch, opt_pair_mma;
+    int eff_schedule;  // the schedule that runs (GEMM_SCHED_AUTO resolved)
     int64_t wait_limit_us;
     int max_pair_ctas;  // CTAs co-resident as 2-CTA clusters (0: unknown)
     // derived
@@ -81,7 +82,7 @@ namespace {
 
 bool valid_enums(int dtype, int la, int lb, int sched) {
     return (dtype == GEMM_F16 || dtype == GEMM_BF16) && (la == 0 || la == 1) &&
-           (lb == 0 || lb == 1) && (sched >= 0 && sched <= 3);
+           (lb == 0 || lb == 1) && (sched >= 0 && sched <= 4);
 }
 
 template <int BN, bool BF, int CM, int AROWS = 128, bool PAIR_MMA = false>
@@ -165,25 +166,59 @@ gemm_status_t derive(gemm_plan* p) {
     const int64_t ipt = cdiv64(p->K, BK);
     if (tiles > INT32_MAX / 2 || ipt > INT32_MAX / 2) return GEMM_ERR_UNSUPPORTED;
 
+    int g_ctas = p->opt_grid > 0 ? p->opt_grid : p->num_sms;
+    if (CM == 2 && p->max_pair_ctas > 0 && g_ctas > p->max_pair_ctas) g_ctas = p->max_pair_ctas;
+    const int g = g_ctas / CM > 0 ? g_ctas / CM : 1;  // scheduling units
+
+    // GEMM_SCHED_AUTO: choose from the shape, after a timed sweep of 30
+    // log-sampled shapes and the five workloads on GB300:
+    //  * one row of tiles (skinny, memory-bound) -> Stream-K, whose units
+    //    start at different k and so spread the B stream;
+    //  * fewer than 8 k-iterations per unit -> persistent (nothing to split);
+    //  * four or more waves of tiles -> persistent (the tail is at most a
+    //    quarter wave, and whole tiles keep the grouped raster's L2 reuse);
+    //  * under one wave -> Stream-K when at most 70% of the units would have
+    //    a tile, else persistent (the fixup costs more than the idle units);
+    //  * one to four waves -> the hybrid rule when each split tile has at most
+    //    8 contributors and tiles have at least 32 k-iterations (it keeps most
+    //    tiles whole), else every tile in the Stream-K wave (a few tiles split
+    //    many ways make their owners add a dozen partials).
+    int sched = p->schedule;
+    int sk_mode = p->opt_sk_mode;
+    if (sched == GEMM_SCHED_AUTO) {
+        const double waves = (double)tiles / g;
+        int64_t sk_h = tiles % g;
+        if (tiles - sk_h > g) sk_h += g;
+        if (tiles_m == 1 && tiles < g) {
+            sched = GEMM_SCHED_STREAMK;
+        } else if (tiles * ipt < 8 * (int64_t)g || waves >= 4.0) {
+            sched = GEMM_SCHED_PERSISTENT;
+        } else if (waves < 1.0) {
+            sched = (tiles * 10 <= 7 * (int64_t)g) ? GEMM_SCHED_STREAMK : GEMM_SCHED_PERSISTENT;
+        } else {
+            sched = GEMM_SCHED_STREAMK;
+            const bool hybrid_ok = sk_h > 0 && g <= 8 * sk_h && ipt >= 32;
+            sk_mode = hybrid_ok ? 0 : 1;
+        }
+    }
+    p->eff_schedule = sched;
+
     Sched s{};
     s.tiles_m = (int32_t)tiles_m;
     s.tiles_n = (int32_t)tiles_n;
     s.tiles = (int32_t)tiles;
     s.ipt = (int32_t)(ipt > 0 ? ipt : 1);
     s.group_m = p->opt_group_m >= 0 ? p->opt_group_m
-                                    : (p->schedule == GEMM_SCHED_DATA_PARALLEL ? 0 : 8);
-    int g_ctas = p->opt_grid > 0 ? p->opt_grid : p->num_sms;
-    if (CM == 2 && p->max_pair_ctas > 0 && g_ctas > p->max_pair_ctas) g_ctas = p->max_pair_ctas;
-    const int g = g_ctas / CM > 0 ? g_ctas / CM : 1;  // scheduling units
+                                    : (sched == GEMM_SCHED_DATA_PARALLEL ? 0 : 8);
     s.sk_tiles = 0;
     s.sk_q = s.sk_r = 0;
-    if (p->schedule == GEMM_SCHED_DATA_PARALLEL) {
+    if (sched == GEMM_SCHED_DATA_PARALLEL) {
         s.grid = s.tiles;
         s.persistent = 0;
-    } else if (p->schedule == GEMM_SCHED_PERSISTENT) {
+    } else if (sched == GEMM_SCHED_PERSISTENT) {
         s.grid = (int32_t)(tiles < g ? tiles : g);
         s.persistent = 1;
-    } else if (p->schedule == GEMM_SCHED_SPLITK) {
+    } else if (sched == GEMM_SCHED_SPLITK) {
         // as many parts as fit in one round of the scheduling units, at most
         // one part per 4 k-iterations
         int64_t S = p->opt_split;
@@ -200,7 +235,7 @@ gemm_status_t derive(gemm_plan* p) {
     } else {
         int64_t sk = tiles % g;
         if (p->opt_two_tiles && tiles - sk > g) sk += g;
-        if (p->opt_sk_mode == 1) sk = tiles;  // every tile in the Stream-K wave
+        if (sk_mode == 1) sk = tiles;  // every tile in the Stream-K wave
         s.sk_tiles = (int32_t)sk;
         s.grid = tiles > 0 ? g : 0;
         s.persistent = 1;
@@ -222,10 +257,10 @@ gemm_status_t derive(gemm_plan* p) {
     p->ctas = s.grid * CM;
     p->stages = stages_for(BN, p->AROWS, p->PAIR);
     p->smem_bytes = smem_for(BN, p->AROWS, p->PAIR);
-    if (p->schedule == GEMM_SCHED_STREAMK && s.sk_tiles > 0) {
+    if (sched == GEMM_SCHED_STREAMK && s.sk_tiles > 0) {
         p->ws_flag_bytes = ((size_t)s.sk_tiles * CM * 8 + 255) / 256 * 256;
         p->ws_bytes = p->ws_flag_bytes + (size_t)p->ctas * BM * BN * sizeof(float);
-    } else if (p->schedule == GEMM_SCHED_SPLITK && s.split > 1) {
+    } else if (sched == GEMM_SCHED_SPLITK && s.split > 1) {
         // one flag per tile half, one partial slot per (tile, part >= 1, half)
         p->ws_flag_bytes = ((size_t)s.tiles * CM * 8 + 255) / 256 * 256;
         p->ws_bytes = p->ws_flag_bytes +
@@ -296,7 +331,7 @@ gemm_status_t make_plan(gemm_plan_t* out, int64_t M, int64_t N, int64_t K, int d
     p->opt_split = 0;
     p->opt_k_rotate = 0;
     p->opt_l2_prefetch = -1;
-    p->opt_pair_mma = 0;
+    p->opt_pair_mma = 1;
     p->wait_limit_us = 1000000;
     if (offline) {
         if (num_sms <= 0) { delete p; return GEMM_ERR_INVALID_ARG; }
@@ -434,7 +469,9 @@ gemm_status_t gemm_plan_set_option(gemm_plan_t p, int key, int64_t value) {
     switch (key) {
         case GEMM_OPT_GRID:
             if (value < 0 || value > 65535) return GEMM_ERR_UNSUPPORTED;
-            if (p->schedule == GEMM_SCHED_STREAMK && value > p->num_sms) return GEMM_ERR_UNSUPPORTED;
+            if ((p->schedule == GEMM_SCHED_STREAMK || p->schedule == GEMM_SCHED_AUTO) &&
+                value > p->num_sms)
+                return GEMM_ERR_UNSUPPORTED;
             p->opt_grid = (int)value;
             break;
         case GEMM_OPT_GROUP_M:
@@ -514,6 +551,8 @@ gemm_status_t gemm_plan_get_info(gemm_plan_t p, int key, int64_t* value) {
         case GEMM_INFO_K_ROTATE: v = p->s.k_rotate; break;
         case GEMM_INFO_L2_PREFETCH: v = p->s.l2_prefetch; break;
         case GEMM_INFO_PAIR_MMA: v = p->PAIR; break;
+        case GEMM_INFO_SCHEDULE: v = p->eff_schedule; break;
+        case GEMM_INFO_SK_MODE: v = (p->eff_schedule == GEMM_SCHED_STREAMK && p->s.sk_tiles == p->s.tiles) ? 1 : 0; break;
         default: return GEMM_ERR_INVALID_ARG;
     }
     *value = v;

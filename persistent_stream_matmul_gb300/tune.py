@@ -1,0 +1,180 @@
+"""Timing sweeps over plan options (device-timed, CUDA events).
+
+* ``grid_sweep``: the Stream-K grid sweep of the GitHub issue "Stream-k matmul
+  implementation very slow ..." (final version, log-sampled benchmark): for
+  each shape, g in {#SM, 2 x #SM, #tiles when below 2 x #SM, ten random even
+  values below 2 x #SM}, each with and without the two_tiles rule.  Grids
+  whose CTAs cannot all be resident at once (more than one CTA per SM) are
+  reported as refused: the owners of split tiles wait on their peers.
+* ``shape_sweep``: the same issue's shape sampler: M, N and K drawn from
+  multiples of 256 spaced evenly in log2 between 256 and 8192, a fixed random
+  sample of the triples (seed 123); each shape timed with every schedule and
+  with GEMM_SCHED_AUTO.
+
+Run as ``python -m persistent_stream_matmul_gb300.tune --help``.  Operands
+are random device data (timing does not depend on the values); correctness
+over sampled shapes is checked by the test suite, not here.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import random
+import statistics
+
+from . import _binding as B
+
+SCHEDULE_VARIANTS = {
+    "dp": ("dp", {}),
+    "persistent": ("persistent", {}),
+    "streamk": ("streamk", {}),
+    "streamk_all": ("streamk", {"sk_mode": 1}),
+    "splitk": ("splitk", {}),
+    "auto": ("auto", {}),
+}
+
+
+def log_sampled_values(lo: int = 256, hi: int = 8192, step: int = 256, n: int = 1000):
+    """Multiples of `step` spaced evenly in log2 between lo and hi, deduplicated."""
+    a, b = math.log2(lo), math.log2(hi)
+    vals = {int(round(2 ** (a + (b - a) * i / (n - 1)) / step)) * step for i in range(n)}
+    return sorted(v for v in vals if v > 0)
+
+
+def sample_shapes(count: int, seed: int = 123, max_macs: float | None = None):
+    """`count` (M, N, K) triples sampled without replacement from all triples."""
+    vals = log_sampled_values()
+    triples = [(m, n, k) for m in vals for n in vals for k in vals]
+    if max_macs:
+        triples = [t for t in triples if t[0] * t[1] * t[2] <= max_macs]
+    return random.Random(seed).sample(triples, count)
+
+
+class Operands:
+    """Random bf16/fp16 device operands, reused across plans of one shape."""
+
+    def __init__(self, M, N, K, torch_mod):
+        t = torch_mod
+        self.M, self.N, self.K = M, N, K
+        self.a = t.randn(M * K, device="cuda").to(t.bfloat16).view(t.int16)
+        self.b = t.randn(K * N, device="cuda").to(t.bfloat16).view(t.int16)
+        self.c = t.empty(M * N, dtype=t.int16, device="cuda")
+        self.t = t
+        self.ws = None
+
+    def workspace(self, nbytes):
+        if nbytes == 0:
+            return None
+        if self.ws is None or self.ws.numel() < nbytes:
+            self.ws = self.t.zeros(nbytes, dtype=self.t.uint8, device="cuda")
+        return self.ws
+
+
+def time_plan(ops: Operands, dtype, la, lb, schedule, options, warmup=3, iters=10):
+    """Median device time (us) of one gemm_run, or a refusal reason."""
+    t = ops.t
+    try:
+        p = B.Plan(ops.M, ops.N, ops.K, dtype, la, lb, schedule, **options)
+    except B.GemmError as e:
+        return {"refused": str(e)}
+    try:
+        w = ops.workspace(p.workspace_size)
+        stream = t.cuda.current_stream()
+        for _ in range(warmup):
+            p.run(ops.a, ops.b, ops.c, w, stream)
+        ev = [t.cuda.Event(enable_timing=True) for _ in range(2 * iters)]
+        for i in range(iters):
+            ev[2 * i].record(stream)
+            p.run(ops.a, ops.b, ops.c, w, stream)
+            ev[2 * i + 1].record(stream)
+        t.cuda.synchronize()
+        st = p.last_status(stream)
+        if st != B.GEMM_OK:
+            return {"refused": B.gemm_status_string(st)}
+        us = statistics.median(ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(iters)) * 1e3
+        flops = 2.0 * ops.M * ops.N * ops.K
+        return {"us": us, "tflops": flops / (us * 1e-6) / 1e12,
+                "schedule": p.info("schedule"), "tile": "%dx%d" % (p.info("tile_m"), p.info("tile_n")),
+                "grid": p.info("grid")}
+    except B.GemmError as e:
+        return {"refused": str(e)}
+    finally:
+        p.close()
+
+
+def grid_sweep(M, N, K, dtype=B.GEMM_BF16, la=0, lb=1, seed=123, torch_mod=None):
+    import torch as t
+    t = torch_mod or t
+    sms = t.cuda.get_device_properties(0).multi_processor_count
+    probe = B.Plan(M, N, K, dtype, la, lb, "streamk")
+    tiles = probe.info("tiles") * probe.info("cluster_m")
+    probe.close()
+    grids = [sms, 2 * sms] + ([tiles] if tiles < 2 * sms else [])
+    grids += random.Random(seed).sample(range(2, 2 * sms, 2), 10)
+    ops = Operands(M, N, K, t)
+    rows = []
+    for two in (1, 0):
+        for g in grids:
+            r = time_plan(ops, dtype, la, lb, "streamk", {"grid": g, "two_tiles": two})
+            rows.append({"M": M, "N": N, "K": K, "grid": g, "two_tiles": two, **r})
+    return rows
+
+
+def shape_sweep(count, dtype=B.GEMM_BF16, la=0, lb=1, seed=123, max_macs=2.0 ** 36,
+                variants=None, torch_mod=None):
+    import torch as t
+    t = torch_mod or t
+    variants = variants or list(SCHEDULE_VARIANTS)
+    rows = []
+    for (M, N, K) in sample_shapes(count, seed, max_macs):
+        ops = Operands(M, N, K, t)
+        res = {}
+        for name in variants:
+            sched, opt = SCHEDULE_VARIANTS[name]
+            res[name] = time_plan(ops, dtype, la, lb, sched, opt)
+        rows.append({"M": M, "N": N, "K": K, "results": res})
+        del ops
+    return rows
+
+
+def summarize_shapes(rows):
+    """Geometric-mean throughput ratios of each variant to the best per shape."""
+    names = list(rows[0]["results"]) if rows else []
+    out = {}
+    for n in names:
+        ratios = []
+        for r in rows:
+            best = max(v.get("tflops", 0.0) for v in r["results"].values())
+            v = r["results"][n].get("tflops")
+            if v and best:
+                ratios.append(v / best)
+        if ratios:
+            out[n] = {"geomean_vs_best": math.exp(sum(math.log(x) for x in ratios) / len(ratios)),
+                      "wins": sum(1 for r in rows if max(r["results"], key=lambda k:
+                                  r["results"][k].get("tflops", 0.0)) == n),
+                      "shapes": len(ratios)}
+    return out
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--grid-sweep", nargs=3, type=int, metavar=("M", "N", "K"))
+    ap.add_argument("--shapes", type=int, default=0, help="log-sampled shapes to time")
+    ap.add_argument("--max-macs", type=float, default=2.0 ** 36)
+    ap.add_argument("--dtype", choices=["bf16", "fp16"], default="bf16")
+    args = ap.parse_args()
+    dtype = B.GEMM_BF16 if args.dtype == "bf16" else B.GEMM_F16
+    B.load()
+    if args.grid_sweep:
+        for row in grid_sweep(*args.grid_sweep, dtype=dtype):
+            print(json.dumps(row), flush=True)
+    if args.shapes:
+        rows = shape_sweep(args.shapes, dtype=dtype, max_macs=args.max_macs)
+        for row in rows:
+            print(json.dumps(row), flush=True)
+        print(json.dumps({"summary": summarize_shapes(rows)}), flush=True)
+
+
+if __name__ == "__main__":
+    main()

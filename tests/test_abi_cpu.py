@@ -155,6 +155,27 @@ def test_splitk_units(lib, M, N, K, cm):
         p.close()
 
 
+def test_auto_schedule_choices(lib):
+    cases = {  # workload -> (schedule, all tiles in the Stream-K wave)
+        (512, 512, 512): (B.GEMM_SCHED_PERSISTENT, 0),
+        (8192, 8192, 8192): (B.GEMM_SCHED_PERSISTENT, 0),
+        (2304, 2304, 8192): (B.GEMM_SCHED_STREAMK, 1),
+        (8192, 14336, 4096): (B.GEMM_SCHED_PERSISTENT, 0),
+        (64, 8192, 8192): (B.GEMM_SCHED_STREAMK, 1),
+        # from the timed sweep of log-sampled shapes
+        (3840, 2816, 5888): (B.GEMM_SCHED_STREAMK, 0),
+        (768, 6656, 2304): (B.GEMM_SCHED_STREAMK, 1),
+        (4352, 512, 5888): (B.GEMM_SCHED_PERSISTENT, 0),
+        (256, 1792, 6400): (B.GEMM_SCHED_STREAMK, 1),
+        (512, 5632, 1280): (B.GEMM_SCHED_STREAMK, 1),
+        (4608, 5120, 1024): (B.GEMM_SCHED_PERSISTENT, 0),
+    }
+    for (M, N, K), (sched, mode) in cases.items():
+        p = B.Plan(M, N, K, B.GEMM_BF16, 0, 1, "auto", offline_sms=152)
+        assert (p.info("schedule"), p.info("sk_mode")) == (sched, mode), (M, N, K)
+        p.close()
+
+
 def test_half_height_a_for_short_m(lib):
     p = B.Plan(64, 8192, 8192, B.GEMM_F16, 0, 0, "streamk", offline_sms=148, tile_n=128)
     assert p.info("a_rows_per_stage") == 64 and p.info("stages") == 8

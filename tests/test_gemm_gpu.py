@@ -13,7 +13,10 @@ from tests.gpu_util import Workspace, ensure_built, run, to_device
 
 pytestmark = pytest.mark.gpu
 
-SCHEDS = ["dp", "persistent", "streamk", "splitk"]
+SCHEDS = ["dp", "persistent", "streamk", "splitk", "auto"]
+# (tile width, CTAs per cluster, pair MMA): every kernel variant
+CONFIGS = [(64, 1, 0), (128, 1, 0), (128, 2, 0), (128, 2, 1), (256, 1, 0), (256, 2, 0),
+           (256, 2, 1)]
 LAYOUTS = [(0, 0), (0, 1), (1, 0), (1, 1)]
 
 
@@ -51,12 +54,12 @@ def test_parity_small(sched, dtype, la, lb):
         if la == 1 and M % 8:
             continue
         A, Bm, dA, dB = _case(M, N, K, dtype, la, lb, ("normal", 1.0), 10 + i)
-        for tile_n in (64, 128, 256):
-            for cm in ((1,) if tile_n == 64 else (1, 2)):
-                p = B.Plan(M, N, K, dtype, la, lb, sched, tile_n=tile_n, cluster_m=cm)
-                Cb = run(p, dA, dB, M, N, ws)
-                _check_full(Cb, A, Bm, M, N, K, dtype, la, lb)
-                p.close()
+        for tile_n, cm, pair in CONFIGS:
+            p = B.Plan(M, N, K, dtype, la, lb, sched, tile_n=tile_n, cluster_m=cm,
+                       pair_mma=pair)
+            Cb = run(p, dA, dB, M, N, ws)
+            _check_full(Cb, A, Bm, M, N, K, dtype, la, lb)
+            p.close()
 
 
 @pytest.mark.parametrize("sched", SCHEDS)
@@ -68,8 +71,8 @@ def test_integer_bit_exact_small(sched, dtype, la, lb):
         if la == 1 and M % 8:
             continue
         A, Bm, dA, dB = _case(M, N, K, dtype, la, lb, inputs.INT_LAW, 50 + i)
-        for cm in (1, 2):
-            p = B.Plan(M, N, K, dtype, la, lb, sched, cluster_m=cm)
+        for cm, pair in ((1, 0), (2, 0), (2, 1)):
+            p = B.Plan(M, N, K, dtype, la, lb, sched, cluster_m=cm, pair_mma=pair)
             Cb = run(p, dA, dB, M, N, ws)
             _check_full(Cb, A, Bm, M, N, K, dtype, la, lb, exact=True)
             p.close()
@@ -83,16 +86,15 @@ def test_streamk_forced_grids_integer(dtype):
     _, _, Cref = oracle.gemm(A, Bm, M, N, K, dtype, 0, 0)
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     ws = Workspace()
-    for tile_n in (64, 128, 256):
-        for cm in ((1,) if tile_n == 64 else (1, 2)):
-            tiles = -(-3 // cm) * (N // tile_n)
-            for g in sorted({2, 8, 14, tiles * cm, sms}):
-                for two in (0, 1):
-                    p = B.Plan(M, N, K, dtype, 0, 0, "streamk", tile_n=tile_n, grid=g,
-                               two_tiles=two, cluster_m=cm)
-                    Cb = run(p, dA, dB, M, N, ws)
-                    assert np.array_equal(Cb, Cref), (tile_n, cm, g, two)
-                    p.close()
+    for tile_n, cm, pair in CONFIGS:
+        tiles = -(-3 // cm) * (N // tile_n)
+        for g in sorted({2, 8, 14, tiles * cm, sms}):
+            for two in (0, 1):
+                p = B.Plan(M, N, K, dtype, 0, 0, "streamk", tile_n=tile_n, grid=g,
+                           two_tiles=two, cluster_m=cm, pair_mma=pair)
+                Cb = run(p, dA, dB, M, N, ws)
+                assert np.array_equal(Cb, Cref), (tile_n, cm, pair, g, two)
+                p.close()
 
 
 @pytest.mark.parametrize("tile_n", [128, 256])
