@@ -73,7 +73,7 @@ struct gemm_plan {
     bool tm_valid;
     CUtensorMap tmA, tmB;
     const void* flags_cleared_for;
-    bool attr_set[20];
+    bool attr_set[24];
     unsigned long long* trace;  // optional per-CTA stamps (caller-owned device buffer)
     size_t trace_bytes;
 };
@@ -99,7 +99,11 @@ void* pick_kernel_cm(int BN, int dtype) {
 
 void* pick_kernel(int BN, int dtype, int CM, int AROWS = 128, int PAIR = 0) {
     const bool bf = dtype == GEMM_BF16;
-    if (PAIR) {  // CM = 2, BN = 128 or 256
+    if (PAIR) {  // CM = 2, BN = 128 or 256, AROWS = 128 or 64
+        if (AROWS == 64) {
+            if (BN == 256) return bf ? kernel_ptr<256, true, 2, 64, true>() : kernel_ptr<256, false, 2, 64, true>();
+            return bf ? kernel_ptr<128, true, 2, 64, true>() : kernel_ptr<128, false, 2, 64, true>();
+        }
         if (BN == 256) return bf ? kernel_ptr<256, true, 2, 128, true>() : kernel_ptr<256, false, 2, 128, true>();
         return bf ? kernel_ptr<128, true, 2, 128, true>() : kernel_ptr<128, false, 2, 128, true>();
     }
@@ -114,19 +118,22 @@ void* pick_kernel(int BN, int dtype, int CM, int AROWS = 128, int PAIR = 0) {
 
 int kernel_index(int BN, int dtype, int CM, int AROWS, int PAIR) {
     const int bf = dtype == GEMM_BF16 ? 1 : 0;
-    if (PAIR) return 14 + 2 * (BN == 256 ? 1 : 0) + bf;
+    if (PAIR) return 14 + 4 * (AROWS == 64 ? 1 : 0) + 2 * (BN == 256 ? 1 : 0) + bf;
     if (BN == 64) return 10 + 2 * (AROWS == 64 ? 1 : 0) + bf;
     if (AROWS == 64) return 8 + bf;
     return (BN == 256 ? 4 : 0) + 2 * bf + (CM == 2 ? 1 : 0);
 }
 
 int smem_for(int BN, int AROWS = 128, int PAIR = 0) {
+    if (PAIR && AROWS == 64)
+        return BN == 256 ? Cfg<256, 64, true>::SMEM_BYTES : Cfg<128, 64, true>::SMEM_BYTES;
     if (PAIR) return BN == 256 ? Cfg<256, 128, true>::SMEM_BYTES : Cfg<128, 128, true>::SMEM_BYTES;
     if (BN == 64) return AROWS == 64 ? Cfg<64, 64>::SMEM_BYTES : Cfg<64>::SMEM_BYTES;
     if (AROWS == 64) return Cfg<128, 64>::SMEM_BYTES;
     return BN == 256 ? Cfg<256>::SMEM_BYTES : Cfg<128>::SMEM_BYTES;
 }
 int stages_for(int BN, int AROWS = 128, int PAIR = 0) {
+    if (PAIR && AROWS == 64) return BN == 256 ? Cfg<256, 64, true>::STAGES : Cfg<128, 64, true>::STAGES;
     if (PAIR) return BN == 256 ? Cfg<256, 128, true>::STAGES : Cfg<128, 128, true>::STAGES;
     if (BN == 64) return AROWS == 64 ? Cfg<64, 64>::STAGES : Cfg<64>::STAGES;
     if (AROWS == 64) return Cfg<128, 64>::STAGES;
@@ -250,10 +257,12 @@ gemm_status_t derive(gemm_plan* p) {
     p->BN = BN;
     p->CM = CM;
     // one row of tiles with at most 64 valid rows: load only those rows of A
-    p->AROWS = (p->M <= 64 && CM == 1 && BN <= 128) ? 64 : 128;
     // pair MMA (tcgen05 cta_group::2) for 2-CTA clusters: each CTA keeps
     // only its half of B, so the ring is deeper
     p->PAIR = (CM == 2 && p->opt_pair_mma == 1) ? 1 : 0;
+    // at most 64 valid rows: load only 64 rows of A per stage (without
+    // clusters for tiles up to 128 wide, or with a pair MMA)
+    p->AROWS = (p->M <= 64 && ((CM == 1 && BN <= 128) || p->PAIR)) ? 64 : 128;
     p->ctas = s.grid * CM;
     p->stages = stages_for(BN, p->AROWS, p->PAIR);
     p->smem_bytes = smem_for(BN, p->AROWS, p->PAIR);

@@ -169,7 +169,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 const __grid_constant__ KParams p) {
     using Cf = Cfg<BN, AROWS, PAIR_MMA>;
     static_assert(!PAIR_MMA || CM == 2, "a pair MMA needs a 2-CTA cluster");
-    static_assert(AROWS == 128 || CM == 1, "half-height A only without clusters");
+    static_assert(AROWS == 128 || CM == 1 || PAIR_MMA, "half-height A: no multicast clusters");
     static_assert(BN >= 128 || CM == 1, "64-wide tiles only without clusters");
     constexpr int STAGES = Cf::STAGES;
     static_assert(CM == 1 || CM == 2, "cluster size");
@@ -302,10 +302,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         const uint32_t fbc = mapa_shared(fb, 0);
                         if (rank == 0) mbar_arrive_expect_tx(fb, 2 * Cf::STAGE_BYTES);
                         if (!p.a_mn) {
-                            tma_load_2d_pair(sa, &tmA, fbc, k_el, m0, pol_a);
+                            tma_load_2d_pair(sa, &tmA, fbc, k_el, m0, pol_a);  // AROWS rows
                         } else {
 #pragma unroll
-                            for (int c = 0; c < BM / 64; ++c)
+                            for (int c = 0; c < AROWS / 64; ++c)
                                 tma_load_2d_pair(sa + c * MN_CHUNK_BYTES, &tmA, fbc, m0 + 64 * c,
                                                  k_el, pol_a);
                         }

@@ -103,7 +103,7 @@ def test_pair_mma(tile_n, sched):
     # 2-CTA clusters issuing one tcgen05 pair MMA (256 x BN) per k-step
     ws = Workspace()
     for i, (M, N, K) in enumerate(((256, 256, 512), (300, 264, 200), (512, 640, 1032),
-                                   (1000, 1040, 2048))):
+                                   (1000, 1040, 2048), (64, 1024, 2048), (40, 512, 1032))):
         for dtype in (inputs.F16, inputs.BF16):
             for la, lb in LAYOUTS:
                 if la == 1 and M % 8:
@@ -113,6 +113,7 @@ def test_pair_mma(tile_n, sched):
                     p = B.Plan(M, N, K, dtype, la, lb, sched, tile_n=tile_n, cluster_m=2,
                                pair_mma=1)
                     assert p.info("pair_mma") == 1 and p.info("tile_m") == 256
+                    assert p.info("a_rows_per_stage") == (64 if M <= 64 else 128)
                     Cb = run(p, dA, dB, M, N, ws)
                     _check_full(Cb, A, Bm, M, N, K, dtype, la, lb,
                                 exact=law == inputs.INT_LAW)
