@@ -138,7 +138,13 @@ enum {
      * 256 x BN) per k-step issued for both CTAs, each CTA holding only its
      * half of B (deeper ring); 0 = each CTA runs its own 128 x BN MMA on a
      * full B tile assembled by TMA multicast. */
-    GEMM_OPT_PAIR_MMA = 12
+    GEMM_OPT_PAIR_MMA = 12,
+    /* tile order: 0 (default) = the grouped raster of GEMM_OPT_GROUP_M (or
+     * linear); 1 = along a Hilbert curve over the tile grid (the blog summary
+     * "Inside NVIDIA GPUs: Anatomy of high performance matmul kernels" lists
+     * Hilbert-curve scheduling).  The order is built on the host and copied
+     * to a small device table owned by the plan when the option is set. */
+    GEMM_OPT_RASTER = 13
 };
 
 /* Keys for gemm_plan_get_info. */
@@ -162,7 +168,8 @@ enum {
     GEMM_INFO_L2_PREFETCH = 20,     /* k-blocks of B prefetched into L2 ahead of the ring */
     GEMM_INFO_PAIR_MMA = 21,        /* 1 when the cluster runs pair MMAs */
     GEMM_INFO_SCHEDULE = 22,        /* the schedule that runs (GEMM_SCHED_AUTO resolved) */
-    GEMM_INFO_SK_MODE = 23          /* 1 when every tile is in the Stream-K wave */
+    GEMM_INFO_SK_MODE = 23,         /* 1 when every tile is in the Stream-K wave */
+    GEMM_INFO_RASTER = 24           /* 0 grouped / linear, 1 Hilbert */
 };
 
 /* Roles of a work unit reported by gemm_plan_units. */

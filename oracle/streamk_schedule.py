@@ -134,3 +134,29 @@ def splitk_parts(ipt: int, S: int):
     decomposition but print no formula; reading: near-equal contiguous parts,
     part p = [floor(p*ipt/S), floor((p+1)*ipt/S)), the first one the owner)."""
     return [(p * ipt // S, (p + 1) * ipt // S) for p in range(S)]
+
+
+def hilbert_curve(order: int):
+    """Cells (x, y) of the Hilbert curve on a 2^order square, in curve order,
+    by the recursive construction: the curve of order n is four copies of the
+    order n-1 curve -- lower left transposed, upper left, upper right, lower
+    right reflected along the anti-diagonal -- joined end to end."""
+    if order == 0:
+        return [(0, 0)]
+    prev = hilbert_curve(order - 1)
+    h = 1 << (order - 1)
+    q1 = [(y, x) for x, y in prev]                         # transpose
+    q2 = [(x, y + h) for x, y in prev]
+    q3 = [(x + h, y + h) for x, y in prev]
+    q4 = [(2 * h - 1 - y, h - 1 - x) for x, y in prev]     # anti-transpose
+    return q1 + q2 + q3 + q4
+
+
+def hilbert_tiles(tiles_m: int, tiles_n: int):
+    """Tile order (row, column) along the Hilbert curve of the smallest
+    power-of-two square covering the grid, keeping the cells inside it
+    (reading of the blog summary's "Hilbert curves" scheduling policy)."""
+    order = 0
+    while (1 << order) < max(tiles_m, tiles_n):
+        order += 1
+    return [(y, x) for x, y in hilbert_curve(order) if y < tiles_m and x < tiles_n]

@@ -5,6 +5,7 @@
 
 #include <atomic>
 #include <cstdio>
+#include <vector>
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
@@ -49,6 +50,44 @@ uint32_t next_epoch() {
 
 int64_t cdiv64(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
+// Cell d of the Hilbert curve over a side x side square (side a power of
+// two), as (x, y): the classic index-to-coordinates walk, which at each scale
+// picks the quadrant from two bits of d and rotates / reflects the lower
+// levels into it.
+void hilbert_cell(int64_t side, int64_t d, int64_t& x, int64_t& y) {
+    x = y = 0;
+    for (int64_t sz = 1; sz < side; sz *= 2) {
+        const int64_t rx = 1 & (d / 2);
+        const int64_t ry = 1 & (d ^ rx);
+        if (ry == 0) {
+            if (rx == 1) {
+                x = sz - 1 - x;
+                y = sz - 1 - y;
+            }
+            const int64_t t = x;
+            x = y;
+            y = t;
+        }
+        x += sz * rx;
+        y += sz * ry;
+        d /= 4;
+    }
+}
+
+// Tile order along the Hilbert curve of the smallest power-of-two square
+// that covers the tile grid, keeping the cells inside it.
+void hilbert_order(int64_t tiles_m, int64_t tiles_n, std::vector<int32_t>& out) {
+    int64_t side = 1;
+    while (side < tiles_m || side < tiles_n) side *= 2;
+    out.clear();
+    out.reserve((size_t)(tiles_m * tiles_n));
+    for (int64_t d = 0; d < side * side; ++d) {
+        int64_t x, y;
+        hilbert_cell(side, d, x, y);
+        if (y < tiles_m && x < tiles_n) out.push_back((int32_t)((y << 16) | x));
+    }
+}
+
 }  // namespace
 
 struct gemm_plan {
@@ -59,6 +98,10 @@ struct gemm_plan {
     int opt_grid, opt_group_m, opt_tile_n, opt_two_tiles, inject_skip, opt_cluster_m, opt_sk_mode;
     int opt_split, opt_k_rotate, opt_l2_prefetch, opt_pair_mma;
     int eff_schedule;  // the schedule that runs (GEMM_SCHED_AUTO resolved)
+    int opt_raster;    // 0: grouped / linear (GROUP_M), 1: Hilbert curve
+    std::vector<int32_t>* raster_host;  // Hilbert order, (row << 16) | column
+    int32_t* raster_dev;                // device copy
+    int64_t raster_tiles;               // entries in both
     int64_t wait_limit_us;
     int max_pair_ctas;  // CTAs co-resident as 2-CTA clusters (0: unknown)
     // derived
@@ -251,6 +294,31 @@ gemm_status_t derive(gemm_plan* p) {
         s.sk_r = iters % g;
     }
     s.k_rotate = p->opt_k_rotate > 0 ? 1 : 0;
+    s.raster_table = nullptr;  // the device / host tables are set where the Sched is used
+    if (p->opt_raster == 1) {
+        if (tiles_m > 65535 || tiles_n > 65535) return GEMM_ERR_UNSUPPORTED;
+        if (!p->raster_host) p->raster_host = new (std::nothrow) std::vector<int32_t>();
+        if (!p->raster_host) return GEMM_ERR_CUDA;
+        hilbert_order(tiles_m, tiles_n, *p->raster_host);
+        if (!p->offline) {
+            // uploaded here, at configuration time, so that running allocates nothing
+            if (p->raster_dev && p->raster_tiles < tiles) {
+                cudaFree(p->raster_dev);
+                p->raster_dev = nullptr;
+            }
+            if (!p->raster_dev && tiles > 0) {
+                if (cudaMalloc(&p->raster_dev, (size_t)tiles * sizeof(int32_t)) != cudaSuccess) {
+                    p->raster_dev = nullptr;
+                    return GEMM_ERR_CUDA;
+                }
+                p->raster_tiles = tiles;
+            }
+            if (tiles > 0 && cudaMemcpy(p->raster_dev, p->raster_host->data(),
+                                        (size_t)tiles * sizeof(int32_t),
+                                        cudaMemcpyHostToDevice) != cudaSuccess)
+                return GEMM_ERR_CUDA;
+        }
+    }
     // off by default: measured slower on a B read once (extra L2 requests)
     s.l2_prefetch = p->opt_l2_prefetch > 0 ? p->opt_l2_prefetch : 0;
     p->s = s;
@@ -341,6 +409,7 @@ gemm_status_t make_plan(gemm_plan_t* out, int64_t M, int64_t N, int64_t K, int d
     p->opt_k_rotate = 0;
     p->opt_l2_prefetch = -1;
     p->opt_pair_mma = 1;
+    p->opt_raster = 0;
     p->wait_limit_us = 1000000;
     if (offline) {
         if (num_sms <= 0) { delete p; return GEMM_ERR_INVALID_ARG; }
@@ -527,11 +596,25 @@ gemm_status_t gemm_plan_set_option(gemm_plan_t p, int key, int64_t value) {
             if (value != 0 && value != 1) return GEMM_ERR_UNSUPPORTED;
             p->opt_pair_mma = (int)value;
             break;
+        case GEMM_OPT_RASTER:
+            if (value != 0 && value != 1) return GEMM_ERR_UNSUPPORTED;
+            p->opt_raster = (int)value;
+            break;
         default:
             return GEMM_ERR_INVALID_ARG;
     }
     gemm_status_t st = derive(p);
-    if (st != GEMM_OK) *p = saved;
+    if (st != GEMM_OK) {
+        // the raster tables are reallocated in place: keep the current ones
+        std::vector<int32_t>* rh = p->raster_host;
+        int32_t* rd = p->raster_dev;
+        int64_t rt = p->raster_tiles;
+        *p = saved;
+        p->raster_host = rh;
+        p->raster_dev = rd;
+        p->raster_tiles = rt;
+        derive(p);  // the saved options derived before; rebuild any table for them
+    }
     return st;
 }
 
@@ -561,6 +644,7 @@ gemm_status_t gemm_plan_get_info(gemm_plan_t p, int key, int64_t* value) {
         case GEMM_INFO_L2_PREFETCH: v = p->s.l2_prefetch; break;
         case GEMM_INFO_PAIR_MMA: v = p->PAIR; break;
         case GEMM_INFO_SCHEDULE: v = p->eff_schedule; break;
+        case GEMM_INFO_RASTER: v = p->opt_raster; break;
         case GEMM_INFO_SK_MODE: v = (p->eff_schedule == GEMM_SCHED_STREAMK && p->s.sk_tiles == p->s.tiles) ? 1 : 0; break;
         default: return GEMM_ERR_INVALID_ARG;
     }
@@ -612,6 +696,7 @@ gemm_status_t gemm_run(gemm_plan_t p, const void* A, const void* B, void* C, voi
 
     KParams kp{};
     kp.s = p->s;
+    kp.s.raster_table = p->opt_raster == 1 ? p->raster_dev : nullptr;
     kp.M = (int32_t)p->M;
     kp.N = (int32_t)p->N;
     kp.K = (int32_t)p->K;
@@ -713,11 +798,13 @@ gemm_status_t gemm_plan_units(gemm_plan_t p, int64_t cta, int32_t* units, int64_
         (max_units > 0 && !units))
         return GEMM_ERR_INVALID_ARG;
     const int32_t unit_cta = (int32_t)(cta / p->CM);  // both CTAs of a pair run the same units
+    Sched hs = p->s;
+    hs.raster_table = (p->opt_raster == 1 && p->raster_host) ? p->raster_host->data() : nullptr;
     Cursor cur;
-    cursor_init(p->s, unit_cta, cur);
+    cursor_init(hs, unit_cta, cur);
     Unit u;
     int64_t n = 0;
-    while (cursor_next(p->s, unit_cta, cur, u)) {
+    while (cursor_next(hs, unit_cta, cur, u)) {
         if (n < max_units) {
             int32_t* o = units + 5 * n;
             o[0] = u.tile;
@@ -742,7 +829,9 @@ gemm_status_t gemm_plan_set_trace(gemm_plan_t p, void* device_buffer, size_t byt
 gemm_status_t gemm_plan_tile_coords(gemm_plan_t p, int64_t tile, int64_t* tile_m, int64_t* tile_n) {
     if (!p || !tile_m || !tile_n || tile < 0 || tile >= p->s.tiles) return GEMM_ERR_INVALID_ARG;
     int32_t tm, tn;
-    tile_coords(p->s, (int32_t)tile, tm, tn);
+    Sched hs = p->s;
+    hs.raster_table = (p->opt_raster == 1 && p->raster_host) ? p->raster_host->data() : nullptr;
+    tile_coords(hs, (int32_t)tile, tm, tn);
     *tile_m = tm;
     *tile_n = tn;
     return GEMM_OK;
@@ -751,6 +840,8 @@ gemm_status_t gemm_plan_tile_coords(gemm_plan_t p, int64_t tile, int64_t* tile_m
 gemm_status_t gemm_plan_destroy(gemm_plan_t p) {
     if (!p) return GEMM_OK;
     if (p->d_status) cudaFree(p->d_status);
+    if (p->raster_dev) cudaFree(p->raster_dev);
+    delete p->raster_host;
     delete p;
     return GEMM_OK;
 }

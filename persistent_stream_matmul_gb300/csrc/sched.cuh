@@ -10,6 +10,10 @@
 //  * full_tiles: whole tiles numbered after the Stream-K tiles;
 //  * swizzle_tile / linear_tile: the raster (grouped by GROUP_M rows, or
 //    row-major).
+// A third raster follows a Hilbert curve (the blog summary "Inside NVIDIA
+// GPUs: Anatomy of high performance matmul kernels" lists Hilbert-curve
+// scheduling among the Hopper tricks): the plan builds the order on the
+// host, and tile_coords reads it from a table.
 // The persistent schedule (HF post "naive vs persistent matmul") is the same
 // machinery with no Stream-K tiles and a grid of one CTA per SM; the
 // data-parallel schedule launches one CTA per tile.
@@ -52,6 +56,7 @@ struct Sched {
     int32_t k_rotate;    // 1: whole tiles start their k loop at their own
                          // offset (see unit_kblock)
     int32_t l2_prefetch; // k-blocks of B to prefetch into L2 ahead of the ring (0: off)
+    const int32_t* raster_table;  // optional: tile id -> (row << 16) | column
     int64_t sk_q;        // Stream-K iterations per CTA (floor)
     int64_t sk_r;        // CTAs [0, sk_r) take sk_q + 1
 };
@@ -89,7 +94,11 @@ PSM_HD int32_t unit_kblock(const Sched& s, int32_t tile, int32_t k0, int32_t k1,
 }
 
 PSM_HD void tile_coords(const Sched& s, int32_t t, int32_t& tm, int32_t& tn) {
-    if (s.group_m > 0) {
+    if (s.raster_table) {
+        const int32_t v = s.raster_table[t];
+        tm = v >> 16;
+        tn = v & 0xFFFF;
+    } else if (s.group_m > 0) {
         int32_t width = s.group_m * s.tiles_n;
         int32_t gid = t / width;
         int32_t first = gid * s.group_m;

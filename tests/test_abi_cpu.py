@@ -280,3 +280,18 @@ def test_owner_peer_structure_on_workloads(lib):
             assert B.ROLE_PEER not in roles[1:]
             assert B.ROLE_OWNER not in roles[:-1]
         p.close()
+
+
+def test_hilbert_raster_matches_oracle(lib):
+    from oracle.streamk_schedule import hilbert_tiles
+    for M, N in ((512, 512), (2304, 2304), (8192, 14336), (64, 8192), (1000, 3000), (384, 128)):
+        for cm in (1, 2):
+            p = B.Plan(M, N, 64, B.GEMM_BF16, 0, 1, "persistent", offline_sms=152, tile_n=128,
+                       cluster_m=cm, raster=1)
+            assert p.info("raster") == 1
+            ref = hilbert_tiles(p.info("tiles_m"), p.info("tiles_n"))
+            assert [p.tile_coords(t) for t in range(p.info("tiles"))] == ref
+            # units follow the same order
+            seen = sorted(u[0] for c in range(0, p.info("grid"), cm) for u in p.units(c))
+            assert seen == list(range(p.info("tiles")))
+            p.close()

@@ -177,6 +177,18 @@ def test_k_rotation_and_l2_prefetch(sched):
                 p.close()
 
 
+@pytest.mark.parametrize("sched", SCHEDS)
+def test_hilbert_raster(sched):
+    ws = Workspace()
+    for (M, N, K), cm in (((1000, 1040, 1032), 1), ((768, 1536, 2048), 2), ((64, 1024, 1024), 1)):
+        A, Bm, dA, dB = _case(M, N, K, inputs.BF16, 0, 1, inputs.INT_LAW, 18)
+        _, _, Cref = oracle.gemm(A, Bm, M, N, K, inputs.BF16, 0, 1)
+        p = B.Plan(M, N, K, inputs.BF16, 0, 1, sched, cluster_m=cm, raster=1)
+        assert p.info("raster") == 1
+        assert np.array_equal(run(p, dA, dB, M, N, ws), Cref)
+        p.close()
+
+
 def test_streamk_deterministic_and_within_bound():
     M, N, K, dtype = 512, 768, 3000 // 8 * 8, inputs.BF16
     A, Bm, dA, dB = _case(M, N, K, dtype, 0, 1, ("normal", 1.0), 8)

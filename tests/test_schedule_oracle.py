@@ -123,3 +123,20 @@ def test_raster_closed_forms():
 
 def test_cdiv():
     assert [cdiv(a, 4) for a in range(0, 10)] == [0, 1, 1, 1, 1, 2, 2, 2, 2, 3]
+
+
+def test_hilbert_curve_closed_forms():
+    from oracle.streamk_schedule import hilbert_curve, hilbert_tiles
+    # the order-1 and order-2 curves, written out by hand
+    assert hilbert_curve(1) == [(0, 0), (0, 1), (1, 1), (1, 0)]
+    assert hilbert_curve(2) == [(0, 0), (1, 0), (1, 1), (0, 1), (0, 2), (0, 3), (1, 3), (1, 2),
+                                (2, 2), (2, 3), (3, 3), (3, 2), (3, 1), (2, 1), (2, 0), (3, 0)]
+    for order in range(1, 7):
+        c = hilbert_curve(order)
+        n = 1 << order
+        assert sorted(c) == [(x, y) for x in range(n) for y in range(n)]
+        # consecutive cells are grid neighbours; the curve runs corner to corner
+        assert all(abs(a[0] - b[0]) + abs(a[1] - b[1]) == 1 for a, b in zip(c, c[1:]))
+        assert c[0] == (0, 0) and c[-1] == (n - 1, 0)
+    t = hilbert_tiles(3, 5)
+    assert sorted(t) == [(m, n) for m in range(3) for n in range(5)]
