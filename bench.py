@@ -25,6 +25,7 @@ import re
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 import numpy as np
@@ -87,11 +88,11 @@ class ClockSampler:
     def __init__(self, device_id: str | None):
         self.proc = None
         self.device_id = device_id
-        self.path = os.path.join(ROOT, "gpurun_out", "clocks_bench_%d.csv" % os.getpid())
+        fd, self.path = tempfile.mkstemp(prefix="psm_clocks_", suffix=".csv")
+        os.close(fd)
 
     def start(self):
         try:
-            os.makedirs(os.path.dirname(self.path), exist_ok=True)
             cmd = ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
                    "-lms", "100"]
             if self.device_id:
@@ -125,6 +126,10 @@ class ClockSampler:
             for name, val in zip(self.REASONS, parts[5:9]):
                 if val.lower().startswith("active"):
                     reasons.add(name)
+        try:
+            os.unlink(self.path)
+        except OSError:
+            pass
         busy = [s for s, p in zip(sm, power) if p > 0.5 * max(power)] if power else sm
         return {"sm_mhz": statistics.median(busy) if busy else None,
                 "sm_max_mhz": max(smax) if smax else None,
