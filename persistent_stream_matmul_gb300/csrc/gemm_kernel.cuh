@@ -68,14 +68,14 @@ struct Cfg {
     // a pair MMA keeps only this CTA's half of the B tile in its ring
     static constexpr int B_STAGE_BYTES = (PAIR_MMA ? BN / 2 : BN) * BK * 2;
     static constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
-    static constexpr int STAGES_FIT = (192 * 1024) / STAGE_BYTES;  // 4, 6, 8 or 12
+    // ring of up to 224 KB (the CTA may hold 227 KB; barriers and alignment
+    // take the rest): 4 stages at BN=256, 7 at BN=128 or with a pair MMA at
+    // BN=256, 9 with half-height A at BN=128, at most 12
+    static constexpr int STAGES_FIT = (224 * 1024) / STAGE_BYTES;
     static constexpr int STAGES = STAGES_FIT > 12 ? 12 : STAGES_FIT;
     static constexpr int TMEM_COLS = 2 * BN;  // two accumulators; 256 or 512
     static constexpr int BAR_BYTES = 256;
-    // A pair MMA reads half tiles through descriptors of full-tile shape: 32 KB
-    // of slack after the ring keeps any read past a half inside this CTA's
-    // shared memory.
-    static constexpr int SLACK_BYTES = PAIR_MMA ? 32 * 1024 : 0;
+    static constexpr int SLACK_BYTES = 0;
     static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + SLACK_BYTES + BAR_BYTES + 1024;
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
     static_assert(BN == 64 || BN == 128 || BN == 256, "tile width");

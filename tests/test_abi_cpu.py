@@ -178,10 +178,10 @@ def test_auto_schedule_choices(lib):
 
 def test_half_height_a_for_short_m(lib):
     p = B.Plan(64, 8192, 8192, B.GEMM_F16, 0, 0, "streamk", offline_sms=148, tile_n=128)
-    assert p.info("a_rows_per_stage") == 64 and p.info("stages") == 8
+    assert p.info("a_rows_per_stage") == 64 and p.info("stages") == 9
     p.close()
     p = B.Plan(65, 8192, 8192, B.GEMM_F16, 0, 0, "streamk", offline_sms=148, tile_n=128)
-    assert p.info("a_rows_per_stage") == 128 and p.info("stages") == 6
+    assert p.info("a_rows_per_stage") == 128 and p.info("stages") == 7
     p.close()
 
 
@@ -227,11 +227,11 @@ def test_default_options(lib):
     p.close()
     p = B.Plan(64, 8192, 8192, B.GEMM_F16, 0, 0, "dp", offline_sms=148)
     assert p.info("tile_n") == 128 and p.info("group_m") == 0 and p.info("tiles") == 64
-    assert p.info("a_rows_per_stage") == 64 and p.info("stages") == 8
+    assert p.info("a_rows_per_stage") == 64 and p.info("stages") == 9
     assert p.info("l2_prefetch") == 0 and p.info("k_rotate") == 0
     p.close()
     p = B.Plan(512, 512, 512, B.GEMM_F16, 0, 0, "dp", offline_sms=148)
-    assert p.info("tile_n") == 64 and p.info("tiles") == 32 and p.info("stages") == 8
+    assert p.info("tile_n") == 64 and p.info("tiles") == 32 and p.info("stages") == 9
     p.close()
     p = B.Plan(2304, 2304, 8192, B.GEMM_BF16, 0, 1, "streamk", offline_sms=152)
     assert p.info("tile_n") == 256 and p.info("cluster_m") == 2 and p.info("tiles") == 81
