@@ -160,8 +160,12 @@ def oracle_rows_gflops(A, Bm, spec, rows):
 def cpu_baseline(A, Bm, spec, target_s=10.0):
     import oracle
     oracle.build()
-    secs, fl = oracle_rows_gflops(A, Bm, spec, 8)
-    rows = int(min(spec["M"], max(8, 8 * target_s / max(secs, 1e-3))))
+    rows = 16
+    secs, fl = oracle_rows_gflops(A, Bm, spec, rows)
+    while secs < 1.0 and rows < spec["M"]:          # probe long enough to use every thread
+        rows = min(spec["M"], rows * 4)
+        secs, fl = oracle_rows_gflops(A, Bm, spec, rows)
+    rows = int(min(spec["M"], max(8, rows * target_s / max(secs, 1e-3))))
     rows = max(8, rows // 8 * 8)
     secs, fl = oracle_rows_gflops(A, Bm, spec, rows)
     return {"value": fl / secs / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(),
