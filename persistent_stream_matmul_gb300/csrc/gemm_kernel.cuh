@@ -501,6 +501,50 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     store = epi_vote_all(got);
                     if (!store && et == 0) record_status(p.status, STATUS_FLAG_TIMEOUT);
                 }
+                // The CTA's last unit: every load into the ring has landed and
+                // every MMA that read it has completed (this accumulator is
+                // ready), so the ring is idle and the epilogue may use it:
+                //  * C: the converted tile is staged in the ring and written
+                //    out row by row (a warp's store covers 512 contiguous
+                //    bytes instead of 16 bytes in each of 32 rows);
+                //  * OWNER: the first `staged` peers' partials of all chunks
+                //    are copied in at once, one round trip to L2 instead of one
+                //    per chunk; the additions keep the ascending k order.
+                // Ring layout: [C: SROWS rows x BN halves, 16-byte units
+                // XOR-swizzled by row][partials: chunk][peer][vec][row] float4.
+                Cursor peek = cur;
+                Unit next_unit;
+                const bool last = !cursor_next(p.s, unit_cta, peek, next_unit);
+                constexpr int SROWS = AROWS;  // rows a CTA can hold valid
+                constexpr int C_UNITS = BN / 8;  // 16-byte units in a staged row
+                constexpr uint32_t C_STAGE_BYTES = (uint32_t)SROWS * BN * 2;
+                constexpr uint32_t PEER_STAGE_BYTES = (uint32_t)BN * SROWS * 4;
+                constexpr uint32_t RING_BYTES = (uint32_t)STAGES * Cf::STAGE_BYTES;
+                static_assert(C_STAGE_BYTES <= RING_BYTES, "C tile fits the ring");
+                const uint32_t pstage = sbase + C_STAGE_BYTES;
+                int staged = 0;
+                if (last) fence_proxy_async_smem();  // the ring was last used by the async proxy
+                if (last && u.role == ROLE_OWNER && store) {
+                    staged = min(u.npeers, (int)((RING_BYTES - C_STAGE_BYTES) / PEER_STAGE_BYTES));
+                    if (row_ok && staged > 0) {
+                        const float4* part = reinterpret_cast<const float4*>(p.partials);
+                        const size_t slot_f4 = (size_t)BM * BN / 4;
+#pragma unroll 1
+                        for (int j = 0; j < BN / 32; ++j) {
+#pragma unroll 1
+                            for (int q = 0; q < staged; ++q) {
+                                const float4* src = part + (size_t)((u.slot + q) * CM + rank) * slot_f4 +
+                                                    (size_t)(j * 8) * BM + row_in_tile;
+                                const uint32_t dst =
+                                    pstage + (uint32_t)((((j * staged + q) * 8) * SROWS + row_in_tile) * 16);
+#pragma unroll
+                                for (int v = 0; v < 8; ++v)
+                                    cp_async_16(dst + (uint32_t)(v * SROWS * 16), src + (size_t)v * BM);
+                            }
+                        }
+                        cp_async_wait_all();
+                    }
+                }
                 uint8_t* crow = reinterpret_cast<uint8_t*>(p.C) + ((size_t)row * p.N) * 2;
 #pragma unroll 1
                 for (int j = 0; j < BN / 32; ++j) {
@@ -511,6 +555,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
                     for (int i = 0; i < 32; ++i) acc[i] = __uint_as_float(r[i]);
                     if (u.role == ROLE_OWNER && store && row_ok) {
+                        // staged peers first (the lowest k), from shared memory
+#pragma unroll 1
+                        for (int q = 0; q < staged; ++q) {
+                            const uint32_t sp =
+                                pstage + (uint32_t)((((j * staged + q) * 8) * SROWS + row_in_tile) * 16);
+#pragma unroll
+                            for (int v = 0; v < 8; ++v) {
+                                const float4 x = ld_shared_f4(sp + (uint32_t)(v * SROWS * 16));
+                                acc[4 * v] += x.x;
+                                acc[4 * v + 1] += x.y;
+                                acc[4 * v + 2] += x.z;
+                                acc[4 * v + 3] += x.w;
+                            }
+                        }
                         // peers in ascending k: slots u.slot, u.slot + 1, ... (this half)
                         // Loads of PEER_BATCH peers are issued before any of them is
                         // added, so 32 16-byte loads per thread are in flight; the
@@ -520,7 +578,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                              (size_t)(j * 8) * BM + row_in_tile;
                         const size_t slot_f4 = (size_t)BM * BN / 4;
 #pragma unroll 1
-                        for (int pp = 1; pp <= u.npeers; pp += PEER_BATCH) {
+                        for (int pp = staged + 1; pp <= u.npeers; pp += PEER_BATCH) {
                             float4 x[PEER_BATCH][8];
 #pragma unroll
                             for (int q = 0; q < PEER_BATCH; ++q) {
@@ -546,15 +604,28 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         }
                     }
                     if (store && row_ok) {
-                        const int col0 = u.tn * BN + j * 32;
+                        if (last) {
+                            const uint32_t srow = sbase + (uint32_t)(row_in_tile * BN * 2);
 #pragma unroll
-                        for (int v = 0; v < 4; ++v) {
-                            const int col = col0 + 8 * v;
-                            if (col < p.N)
-                                st_u4(crow + (size_t)col * 2, pack2<OUT_BF16>(acc[8 * v], acc[8 * v + 1]),
-                                      pack2<OUT_BF16>(acc[8 * v + 2], acc[8 * v + 3]),
-                                      pack2<OUT_BF16>(acc[8 * v + 4], acc[8 * v + 5]),
-                                      pack2<OUT_BF16>(acc[8 * v + 6], acc[8 * v + 7]));
+                            for (int v = 0; v < 4; ++v) {
+                                const int unit = (j * 4 + v) ^ (row_in_tile & (C_UNITS - 1));
+                                st_shared_u4(srow + (uint32_t)(unit * 16),
+                                             pack2<OUT_BF16>(acc[8 * v], acc[8 * v + 1]),
+                                             pack2<OUT_BF16>(acc[8 * v + 2], acc[8 * v + 3]),
+                                             pack2<OUT_BF16>(acc[8 * v + 4], acc[8 * v + 5]),
+                                             pack2<OUT_BF16>(acc[8 * v + 6], acc[8 * v + 7]));
+                            }
+                        } else {
+                            const int col0 = u.tn * BN + j * 32;
+#pragma unroll
+                            for (int v = 0; v < 4; ++v) {
+                                const int col = col0 + 8 * v;
+                                if (col < p.N)
+                                    st_u4(crow + (size_t)col * 2, pack2<OUT_BF16>(acc[8 * v], acc[8 * v + 1]),
+                                          pack2<OUT_BF16>(acc[8 * v + 2], acc[8 * v + 3]),
+                                          pack2<OUT_BF16>(acc[8 * v + 4], acc[8 * v + 5]),
+                                          pack2<OUT_BF16>(acc[8 * v + 6], acc[8 * v + 7]));
+                            }
                         }
                     }
                 }
@@ -565,6 +636,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         mbar_arrive_cluster(mapa_shared(tempty_bar(buf), 0));
                     else
                         mbar_arrive(tempty_bar(buf));
+                }
+                if (last && store) {
+                    // every epilogue warp has staged its rows; write whole rows:
+                    // lane l takes unit l % C_UNITS of row i * (32 / C_UNITS) + l / C_UNITS
+                    named_bar_sync(BAR_EPI_SYNC, EPI_THREADS);
+                    constexpr int ROWS_PER_STORE = 32 / C_UNITS;
+                    const int unit = lane % C_UNITS;
+                    const int col = u.tn * BN + unit * 8;
+                    const int first = (et >> 5) * ROWS_PER_STORE + lane / C_UNITS;
+#pragma unroll 4
+                    for (int r = first; r < rows_valid; r += 4 * ROWS_PER_STORE) {
+                        const uint4 v = ld_shared_u4(sbase + (uint32_t)(r * BN * 2) +
+                                                     (uint32_t)((unit ^ (r & (C_UNITS - 1))) * 16));
+                        if (col < p.N)
+                            st_u4(reinterpret_cast<uint8_t*>(p.C) + ((size_t)(tm * BM + r) * p.N + col) * 2,
+                                  v.x, v.y, v.z, v.w);
+                    }
                 }
             }
             ++iter;
