@@ -497,7 +497,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 bool store = true;
                 if (u.role == ROLE_OWNER) {
                     const uint64_t target = ((uint64_t)p.epoch << 32) | (uint32_t)u.npeers;
-                    bool got = wait_flag(p.flags + u.tile * CM + rank, target, p.wait_limit_ns);
+                    // one thread polls (128 pollers per owner slowed the L2);
+                    // the vote is the barrier that orders the other threads'
+                    // reads of the partials after its acquire
+                    const bool got = et != 0 || wait_flag(p.flags + u.tile * CM + rank, target, p.wait_limit_ns);
                     store = epi_vote_all(got);
                     if (!store && et == 0) record_status(p.status, STATUS_FLAG_TIMEOUT);
                 }
