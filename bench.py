@@ -384,7 +384,8 @@ def main():
         e2e = {"value": whole_job_tflops(flops, n_e2e, world, te),
                "unit": "TFLOP/s", "steps": n_e2e,
                "h2d_bytes_per_step": int(hA.numel() * 2 + hB.numel() * 2),
-               "d2h_bytes_per_step": int(hC.numel() * 2)}
+               "d2h_bytes_per_step": int(hC.numel() * 2),
+               "host_chunks": p.info("host_chunks")}
 
     clocks = sampler.stop()
 

@@ -144,7 +144,14 @@ enum {
      * "Inside NVIDIA GPUs: Anatomy of high performance matmul kernels" lists
      * Hilbert-curve scheduling).  The order is built on the host and copied
      * to a small device table owned by the plan when the option is set. */
-    GEMM_OPT_RASTER = 13
+    GEMM_OPT_RASTER = 13,
+    /* gemm_run_host: 0 (default) = pipelined in 4 row chunks when M >= 2048,
+     * else serial; 1 = always serial; 2..16 = that many row chunks (each a
+     * whole number of scheduled tile rows, so fewer may result).  Serial
+     * whenever the chunks' sub-plans would need more workspace than
+     * gemm_workspace_size of this plan.  GEMM_INFO_HOST_CHUNKS reports the
+     * count gemm_run_host uses. */
+    GEMM_OPT_HOST_CHUNKS = 14
 };
 
 /* Keys for gemm_plan_get_info. */
@@ -169,7 +176,8 @@ enum {
     GEMM_INFO_PAIR_MMA = 21,        /* 1 when the cluster runs pair MMAs */
     GEMM_INFO_SCHEDULE = 22,        /* the schedule that runs (GEMM_SCHED_AUTO resolved) */
     GEMM_INFO_SK_MODE = 23,         /* 1 when every tile is in the Stream-K wave */
-    GEMM_INFO_RASTER = 24           /* 0 grouped / linear, 1 Hilbert */
+    GEMM_INFO_RASTER = 24,          /* 0 grouped / linear, 1 Hilbert */
+    GEMM_INFO_HOST_CHUNKS = 25      /* row chunks gemm_run_host pipelines (1 = serial) */
 };
 
 /* Roles of a work unit reported by gemm_plan_units. */
@@ -228,9 +236,22 @@ gemm_status_t gemm_run(gemm_plan_t plan, const void *A, const void *B, void *C,
 
 /*
  * End-to-end variant: copies hA -> dA and hB -> dB (host to device), runs
- * gemm_run(dA, dB, dC), and copies dC -> hC (device to host), all enqueued on
- * `stream`.  Host buffers should be pinned for the copies to be asynchronous.
- * The caller owns all six buffers; nothing is allocated.  Errors: as gemm_run.
+ * C = A * B on the device copies, and copies dC -> hC (device to host).  All
+ * six buffers are the caller's, in the layouts of the plan; host buffers
+ * should be pinned for the copies to be asynchronous.
+ *  - Serial (GEMM_INFO_HOST_CHUNKS == 1): the three steps are enqueued on
+ *    `stream`, the product through gemm_run.
+ *  - Pipelined (GEMM_INFO_HOST_CHUNKS == n > 1, see GEMM_OPT_HOST_CHUNKS): B
+ *    and then n row chunks of A are copied on an internal stream, chunk i of
+ *    C is computed on `stream` once chunk i of A has arrived, and copied out
+ *    on a second internal stream, so copies and compute overlap.  The call
+ *    records an event on `stream` before its first copy and makes `stream`
+ *    wait for the last copy out, so everything enqueued on `stream` before
+ *    the call precedes it and everything after it follows it.  The first
+ *    pipelined call of a plan creates the two streams, the events and two
+ *    internal sub-plans (released by gemm_plan_destroy or an option change);
+ *    the chunks run one after another on `stream` and share `workspace`.
+ * Errors: as gemm_run; CUDA when a copy, stream or event call fails.
  */
 gemm_status_t gemm_run_host(gemm_plan_t plan, const void *hA, const void *hB, void *hC,
                             void *dA, void *dB, void *dC, void *workspace,

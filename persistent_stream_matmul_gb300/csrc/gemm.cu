@@ -3,6 +3,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cstdio>
 #include <vector>
@@ -103,6 +104,16 @@ struct gemm_plan {
     int32_t* raster_dev;                // device copy
     int64_t raster_tiles;               // entries in both
     int64_t wait_limit_us;
+    int64_t a_ld;         // leading dimension of a column-major A in elements (0: M)
+    int opt_host_chunks;  // gemm_run_host: 0 auto, 1 serial, 2..16 row chunks
+    // gemm_run_host pipeline, made on its first pipelined call
+    gemm_plan* sub_full;  // sub-plan over a full chunk of rows
+    gemm_plan* sub_last;  // sub-plan over the last (shorter) chunk, or null
+    int64_t sub_rows;     // rows of a full chunk
+    cudaStream_t h2d, d2h;
+    cudaEvent_t ev_start, ev_done, ev_a[16], ev_c[16];
+    bool pipe_ready;
+    bool owns_status;     // false for a sub-plan: it reports into its parent's word
     int max_pair_ctas;  // CTAs co-resident as 2-CTA clusters (0: unknown)
     // derived
     int BN, CM, AROWS, PAIR, ctas, stages, smem_bytes;
@@ -411,6 +422,9 @@ gemm_status_t make_plan(gemm_plan_t* out, int64_t M, int64_t N, int64_t K, int d
     p->opt_pair_mma = 1;
     p->opt_raster = 0;
     p->wait_limit_us = 1000000;
+    p->a_ld = 0;
+    p->opt_host_chunks = 0;
+    p->owns_status = true;
     if (offline) {
         if (num_sms <= 0) { delete p; return GEMM_ERR_INVALID_ARG; }
         p->device = -1;
@@ -478,7 +492,7 @@ gemm_status_t encode_maps(gemm_plan* p, const void* A, const void* B) {
             box[0] = BK; box[1] = (cuuint32_t)p->AROWS;
         } else {
             dims[0] = (cuuint64_t)p->M; dims[1] = (cuuint64_t)p->K;
-            strides[0] = (cuuint64_t)p->M * 2;
+            strides[0] = (cuuint64_t)(p->a_ld ? p->a_ld : p->M) * 2;
             box[0] = 64; box[1] = BK;
         }
         if (enc(&p->tmA, dt, 2, const_cast<void*>(A), dims, strides, box, estr,
@@ -523,6 +537,151 @@ struct DeviceGuard {
         if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
     }
 };
+
+gemm_status_t run_impl(gemm_plan_t p, const void* A, const void* B, void* C, void* workspace,
+                       gemm_stream_t stream, bool pdl);
+
+// Options of a sub-plan over some rows of the parent's product: the same
+// tile shape, cluster, schedule and options; A keeps the parent's leading
+// dimension.
+void sub_options(const gemm_plan* p, gemm_plan* sp) {
+    sp->opt_grid = p->opt_grid;
+    sp->opt_group_m = p->opt_group_m;
+    sp->opt_tile_n = p->BN;
+    sp->opt_two_tiles = p->opt_two_tiles;
+    sp->opt_cluster_m = p->CM;
+    sp->opt_sk_mode = p->opt_sk_mode;
+    sp->opt_split = p->opt_split;
+    sp->opt_k_rotate = p->opt_k_rotate;
+    sp->opt_l2_prefetch = p->opt_l2_prefetch;
+    sp->opt_pair_mma = p->opt_pair_mma;
+    sp->wait_limit_us = p->wait_limit_us;
+    sp->a_ld = p->layout_a == GEMM_COL_MAJOR ? (p->a_ld ? p->a_ld : p->M) : 0;
+}
+
+// Workspace of a sub-plan over `rows` rows, from a scratch copy of the plan
+// (no raster table: it does not change the sizes and the copy builds none).
+bool sub_workspace(const gemm_plan* p, int64_t rows, size_t* flag_bytes, size_t* part_bytes) {
+    gemm_plan tmp = *p;
+    tmp.raster_host = nullptr;
+    tmp.raster_dev = nullptr;
+    tmp.opt_raster = 0;
+    tmp.M = rows;
+    tmp.schedule = p->eff_schedule;
+    sub_options(p, &tmp);
+    if (derive(&tmp) != GEMM_OK) return false;
+    *flag_bytes = tmp.ws_flag_bytes;
+    *part_bytes = tmp.ws_bytes - tmp.ws_flag_bytes;
+    return true;
+}
+
+// gemm_run_host: rows per chunk and chunk count.  Pipelining needs enough
+// rows for the copies of one chunk to hide the compute of another, and the
+// sub-plans must fit the plan's workspace: their partials after one flag
+// region as large as either needs.
+int host_chunks(const gemm_plan* p, int64_t* rows_out) {
+    int n = 1;
+    if (p->opt_host_chunks != 1 && p->M > 0 && p->N > 0 && p->K > 0) {
+        if (p->opt_host_chunks >= 2)
+            n = p->opt_host_chunks;
+        else if (p->M >= 2048)
+            n = 4;
+    }
+    int64_t rows = p->M;
+    if (n > 1) {
+        const int64_t unit = (int64_t)BM * p->CM;  // whole scheduled tiles per chunk
+        rows = (p->M + n - 1) / n;
+        rows = (rows + unit - 1) / unit * unit;
+        n = (int)((p->M + rows - 1) / rows);
+    }
+    if (n > 1 && p->ws_bytes > 0) {
+        size_t f1 = 0, q1 = 0, f2 = 0, q2 = 0;
+        bool ok = sub_workspace(p, rows, &f1, &q1);
+        if (ok && p->M % rows) ok = sub_workspace(p, p->M % rows, &f2, &q2);
+        if (!ok || std::max(f1, f2) + std::max(q1, q2) > p->ws_bytes) n = 1;
+    }
+    if (n <= 1) {
+        n = 1;
+        rows = p->M;
+    }
+    if (rows_out) *rows_out = rows;
+    return n;
+}
+
+// A sub-plan over `rows` rows; device errors land in the parent's status word.
+gemm_status_t make_sub(gemm_plan* p, int64_t rows, gemm_plan** out) {
+    gemm_plan* sp = nullptr;
+    gemm_status_t st = make_plan(&sp, rows, p->N, p->K, p->dtype, p->layout_a, p->layout_b,
+                                 p->eff_schedule, 0, 0);
+    if (st != GEMM_OK) return st;
+    sub_options(p, sp);
+    sp->opt_raster = p->opt_raster;
+    st = derive(sp);
+    if (st != GEMM_OK) {
+        gemm_plan_destroy(sp);
+        return st;
+    }
+    cudaFree(sp->d_status);
+    sp->d_status = p->d_status;
+    sp->owns_status = false;
+    *out = sp;
+    return GEMM_OK;
+}
+
+void pipe_release(gemm_plan* p) {
+    if (p->sub_full) gemm_plan_destroy(p->sub_full);
+    if (p->sub_last) gemm_plan_destroy(p->sub_last);
+    p->sub_full = p->sub_last = nullptr;
+    if (p->pipe_ready) {
+        cudaStreamDestroy(p->h2d);
+        cudaStreamDestroy(p->d2h);
+        cudaEventDestroy(p->ev_start);
+        cudaEventDestroy(p->ev_done);
+        for (int i = 0; i < 16; ++i) {
+            cudaEventDestroy(p->ev_a[i]);
+            cudaEventDestroy(p->ev_c[i]);
+        }
+    }
+    p->pipe_ready = false;
+    p->sub_rows = 0;
+}
+
+gemm_status_t pipe_prepare(gemm_plan* p, int64_t rows) {
+    if (p->pipe_ready && p->sub_rows == rows) return GEMM_OK;
+    pipe_release(p);
+    const unsigned ev_flags = cudaEventDisableTiming;
+    bool ok = cudaStreamCreateWithFlags(&p->h2d, cudaStreamNonBlocking) == cudaSuccess;
+    ok = ok && cudaStreamCreateWithFlags(&p->d2h, cudaStreamNonBlocking) == cudaSuccess;
+    ok = ok && cudaEventCreateWithFlags(&p->ev_start, ev_flags) == cudaSuccess;
+    ok = ok && cudaEventCreateWithFlags(&p->ev_done, ev_flags) == cudaSuccess;
+    for (int i = 0; i < 16 && ok; ++i)
+        ok = cudaEventCreateWithFlags(&p->ev_a[i], ev_flags) == cudaSuccess &&
+             cudaEventCreateWithFlags(&p->ev_c[i], ev_flags) == cudaSuccess;
+    if (!ok) {
+        cudaGetLastError();
+        return GEMM_ERR_CUDA;  // the plan keeps pipe_ready = false; what was made leaks
+    }
+    p->pipe_ready = true;
+    p->sub_rows = rows;
+    gemm_status_t st = make_sub(p, rows, &p->sub_full);
+    if (st == GEMM_OK && p->M % rows) st = make_sub(p, p->M % rows, &p->sub_last);
+    if (st != GEMM_OK) {
+        pipe_release(p);
+        return st;
+    }
+    // both sub-plans share the caller's workspace: one flag region, as large
+    // as either needs, then the partials (host_chunks checked that it fits)
+    gemm_plan* subs[2] = {p->sub_full, p->sub_last};
+    size_t flags = 0;
+    for (gemm_plan* sp : subs)
+        if (sp) flags = std::max(flags, sp->ws_flag_bytes);
+    for (gemm_plan* sp : subs)
+        if (sp && sp->ws_bytes > 0) {
+            sp->ws_bytes = flags + (sp->ws_bytes - sp->ws_flag_bytes);
+            sp->ws_flag_bytes = flags;
+        }
+    return GEMM_OK;
+}
 
 }  // namespace
 
@@ -600,6 +759,10 @@ gemm_status_t gemm_plan_set_option(gemm_plan_t p, int key, int64_t value) {
             if (value != 0 && value != 1) return GEMM_ERR_UNSUPPORTED;
             p->opt_raster = (int)value;
             break;
+        case GEMM_OPT_HOST_CHUNKS:
+            if (value < 0 || value > 16) return GEMM_ERR_UNSUPPORTED;
+            p->opt_host_chunks = (int)value;
+            break;
         default:
             return GEMM_ERR_INVALID_ARG;
     }
@@ -614,6 +777,8 @@ gemm_status_t gemm_plan_set_option(gemm_plan_t p, int key, int64_t value) {
         p->raster_dev = rd;
         p->raster_tiles = rt;
         derive(p);  // the saved options derived before; rebuild any table for them
+    } else {
+        pipe_release(p);  // sub-plans follow the options: rebuilt on next use
     }
     return st;
 }
@@ -645,6 +810,7 @@ gemm_status_t gemm_plan_get_info(gemm_plan_t p, int key, int64_t* value) {
         case GEMM_INFO_PAIR_MMA: v = p->PAIR; break;
         case GEMM_INFO_SCHEDULE: v = p->eff_schedule; break;
         case GEMM_INFO_RASTER: v = p->opt_raster; break;
+        case GEMM_INFO_HOST_CHUNKS: v = host_chunks(p, nullptr); break;
         case GEMM_INFO_SK_MODE: v = (p->eff_schedule == GEMM_SCHED_STREAMK && p->s.sk_tiles == p->s.tiles) ? 1 : 0; break;
         default: return GEMM_ERR_INVALID_ARG;
     }
@@ -660,6 +826,15 @@ gemm_status_t gemm_workspace_size(gemm_plan_t p, size_t* bytes) {
 
 gemm_status_t gemm_run(gemm_plan_t p, const void* A, const void* B, void* C, void* workspace,
                        gemm_stream_t stream) {
+    return run_impl(p, A, B, C, workspace, stream, true);
+}
+
+}  // extern "C"
+
+namespace {
+
+gemm_status_t run_impl(gemm_plan_t p, const void* A, const void* B, void* C, void* workspace,
+                       gemm_stream_t stream, bool pdl) {
     if (!p) return GEMM_ERR_INVALID_ARG;
     if (p->offline) return GEMM_ERR_NO_DEVICE;
     if (p->M == 0 || p->N == 0) return GEMM_OK;
@@ -674,7 +849,7 @@ gemm_status_t gemm_run(gemm_plan_t p, const void* A, const void* B, void* C, voi
     }
     if (!A || !B) return GEMM_ERR_INVALID_ARG;
     if (((uintptr_t)A & 15u) || ((uintptr_t)B & 15u) || (p->K % 8) ||
-        (p->layout_a == GEMM_COL_MAJOR && (p->M % 8)))
+        (p->layout_a == GEMM_COL_MAJOR && ((p->a_ld ? p->a_ld : p->M) % 8)))
         return GEMM_ERR_UNSUPPORTED;
     if (p->ws_bytes > 0 && (!workspace || ((uintptr_t)workspace & 15u))) return GEMM_ERR_WORKSPACE;
 
@@ -732,10 +907,13 @@ gemm_status_t gemm_run(gemm_plan_t p, const void* A, const void* B, void* C, voi
     }
     // Programmatic dependent launch: this grid may start while the previous
     // kernel in the stream drains; the kernel waits (griddepcontrol.wait)
-    // before touching global memory.
-    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[na].val.programmaticStreamSerializationAllowed = 1;
-    ++na;
+    // before touching global memory.  Off for the host pipeline's chunks,
+    // which follow event waits on their input copies.
+    if (pdl) {
+        attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[na].val.programmaticStreamSerializationAllowed = 1;
+        ++na;
+    }
     // Stream-K owners wait on peers with higher CTA indices, which never
     // wait themselves.  The grid is at most one CTA per SM (one CTA fits per
     // SM; cluster grids are sized to cudaOccupancyMaxActiveClusters), so every
@@ -752,6 +930,10 @@ gemm_status_t gemm_run(gemm_plan_t p, const void* A, const void* B, void* C, voi
     return GEMM_OK;
 }
 
+}  // namespace
+
+extern "C" {
+
 gemm_status_t gemm_run_host(gemm_plan_t p, const void* hA, const void* hB, void* hC, void* dA,
                             void* dB, void* dC, void* workspace, gemm_stream_t stream) {
     if (!p) return GEMM_ERR_INVALID_ARG;
@@ -763,15 +945,67 @@ gemm_status_t gemm_run_host(gemm_plan_t p, const void* hA, const void* hB, void*
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     const size_t a_bytes = (size_t)p->M * p->K * 2, b_bytes = (size_t)p->K * p->N * 2;
     const size_t c_bytes = (size_t)p->M * p->N * 2;
-    if (p->K > 0) {
-        if (cudaMemcpyAsync(dA, hA, a_bytes, cudaMemcpyHostToDevice, st) != cudaSuccess ||
-            cudaMemcpyAsync(dB, hB, b_bytes, cudaMemcpyHostToDevice, st) != cudaSuccess)
+    int64_t rows = 0;
+    const int chunks = host_chunks(p, &rows);
+    if (chunks <= 1) {
+        if (p->K > 0) {
+            if (cudaMemcpyAsync(dA, hA, a_bytes, cudaMemcpyHostToDevice, st) != cudaSuccess ||
+                cudaMemcpyAsync(dB, hB, b_bytes, cudaMemcpyHostToDevice, st) != cudaSuccess)
+                return GEMM_ERR_CUDA;
+        }
+        gemm_status_t r = gemm_run(p, dA, dB, dC, workspace, stream);
+        if (r != GEMM_OK) return r;
+        if (cudaMemcpyAsync(hC, dC, c_bytes, cudaMemcpyDeviceToHost, st) != cudaSuccess)
             return GEMM_ERR_CUDA;
+        return GEMM_OK;
     }
-    gemm_status_t r = gemm_run(p, dA, dB, dC, workspace, stream);
-    if (r != GEMM_OK) return r;
-    if (cudaMemcpyAsync(hC, dC, c_bytes, cudaMemcpyDeviceToHost, st) != cudaSuccess)
-        return GEMM_ERR_CUDA;
+    // Pipelined: B in, then row chunk i of A in (copy stream) -> chunk i of
+    // C computed (caller's stream) -> chunk i of C out (second copy stream),
+    // so the three overlap across chunks.  Entry and exit are ordered with
+    // the caller's stream through events.
+    gemm_status_t ps = pipe_prepare(p, rows);
+    if (ps != GEMM_OK) return ps;
+    const bool a_col = p->layout_a == GEMM_COL_MAJOR;
+    const char* ha = static_cast<const char*>(hA);
+    char* da = static_cast<char*>(dA);
+    char* hc = static_cast<char*>(hC);
+    char* dc = static_cast<char*>(dC);
+#define PSM_CUDA(x) do { if ((x) != cudaSuccess) return GEMM_ERR_CUDA; } while (0)
+    PSM_CUDA(cudaEventRecord(p->ev_start, st));
+    PSM_CUDA(cudaStreamWaitEvent(p->h2d, p->ev_start, 0));
+    PSM_CUDA(cudaStreamWaitEvent(p->d2h, p->ev_start, 0));
+    PSM_CUDA(cudaMemcpyAsync(dB, hB, b_bytes, cudaMemcpyHostToDevice, p->h2d));
+    for (int i = 0; i < chunks; ++i) {
+        const int64_t r0 = (int64_t)i * rows, nr = std::min(rows, p->M - r0);
+        if (!a_col) {
+            const size_t off = (size_t)r0 * p->K * 2;
+            PSM_CUDA(cudaMemcpyAsync(da + off, ha + off, (size_t)nr * p->K * 2, cudaMemcpyHostToDevice,
+                                     p->h2d));
+        } else {  // rows r0 .. r0+nr-1 of every column
+            PSM_CUDA(cudaMemcpy2DAsync(da + (size_t)r0 * 2, (size_t)p->M * 2, ha + (size_t)r0 * 2,
+                                       (size_t)p->M * 2, (size_t)nr * 2, (size_t)p->K,
+                                       cudaMemcpyHostToDevice, p->h2d));
+        }
+        PSM_CUDA(cudaEventRecord(p->ev_a[i], p->h2d));
+    }
+    for (int i = 0; i < chunks; ++i) {
+        const int64_t r0 = (int64_t)i * rows;
+        gemm_plan* sp = (i == chunks - 1 && p->sub_last) ? p->sub_last : p->sub_full;
+        const void* a_chunk = a_col ? (const void*)(da + (size_t)r0 * 2) : (const void*)(da + (size_t)r0 * p->K * 2);
+        PSM_CUDA(cudaStreamWaitEvent(st, p->ev_a[i], 0));
+        gemm_status_t r = run_impl(sp, a_chunk, dB, dc + (size_t)r0 * p->N * 2, workspace, stream, false);
+        if (r != GEMM_OK) return r;
+        PSM_CUDA(cudaEventRecord(p->ev_c[i], st));
+    }
+    for (int i = 0; i < chunks; ++i) {
+        const int64_t r0 = (int64_t)i * rows, nr = std::min(rows, p->M - r0);
+        PSM_CUDA(cudaStreamWaitEvent(p->d2h, p->ev_c[i], 0));
+        const size_t off = (size_t)r0 * p->N * 2;
+        PSM_CUDA(cudaMemcpyAsync(hc + off, dc + off, (size_t)nr * p->N * 2, cudaMemcpyDeviceToHost, p->d2h));
+    }
+    PSM_CUDA(cudaEventRecord(p->ev_done, p->d2h));
+    PSM_CUDA(cudaStreamWaitEvent(st, p->ev_done, 0));
+#undef PSM_CUDA
     return GEMM_OK;
 }
 
@@ -839,7 +1073,8 @@ gemm_status_t gemm_plan_tile_coords(gemm_plan_t p, int64_t tile, int64_t* tile_m
 
 gemm_status_t gemm_plan_destroy(gemm_plan_t p) {
     if (!p) return GEMM_OK;
-    if (p->d_status) cudaFree(p->d_status);
+    pipe_release(p);
+    if (p->d_status && p->owns_status) cudaFree(p->d_status);
     if (p->raster_dev) cudaFree(p->raster_dev);
     delete p->raster_host;
     delete p;

@@ -295,3 +295,30 @@ def test_hilbert_raster_matches_oracle(lib):
             seen = sorted(u[0] for c in range(0, p.info("grid"), cm) for u in p.units(c))
             assert seen == list(range(p.info("tiles")))
             p.close()
+
+
+def test_host_chunk_policy(lib):
+    """gemm_run_host pipelines whole-tile row chunks; the count follows
+    GEMM_OPT_HOST_CHUNKS, and it stays serial where the chunks' sub-plans
+    would not fit the plan's workspace."""
+    def chunks(M, sched, **opt):
+        p = B.Plan(M, 4096, 4096, B.GEMM_BF16, 0, 1, sched, offline_sms=152, **opt)
+        n = p.info("host_chunks")
+        rows = p.info("tile_m")
+        p.close()
+        return n, rows
+    assert chunks(8192, "persistent")[0] == 4
+    assert chunks(8192, "dp")[0] == 4
+    assert chunks(8192, "auto")[0] == 4          # AUTO resolves to persistent here
+    assert chunks(2047, "persistent")[0] == 1    # too few rows for the default
+    assert chunks(8192, "streamk")[0] == 4       # sub-plans fit the plan's workspace
+    assert chunks(8192, "splitk")[0] == 4
+    assert chunks(8192, "persistent", host_chunks=1)[0] == 1
+    # chunk rows round up to whole scheduled tiles: 1000 rows in 256-row tiles
+    # -> 3 requested chunks of 512 rows become 2
+    n, tm = chunks(1000, "persistent", host_chunks=3, cluster_m=2)
+    assert tm == 256 and n == 2
+    n, tm = chunks(1000, "persistent", host_chunks=16, cluster_m=1, tile_n=128)
+    assert tm == 128 and n == 8
+    with pytest.raises(B.GemmError):
+        chunks(1000, "persistent", host_chunks=17)

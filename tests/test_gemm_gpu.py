@@ -317,6 +317,38 @@ def test_trace_stamps_are_ordered(sched):
     p.close()
 
 
+@pytest.mark.parametrize("la,lb", [(0, 1), (1, 0)])
+def test_run_host_pipelined_chunks(la, lb):
+    # row chunks of A in, chunks of C computed and copied out while the next
+    # chunk's copy runs; a ragged last chunk; the same bytes as gemm_run
+    M, N, K, dtype = 1000, 520, 776, inputs.BF16
+    A, Bm = inputs.operands(M, N, K, dtype, la, lb, inputs.INT_LAW, inputs.INT_LAW, 46)
+    _, _, Cref = oracle.gemm(A, Bm, M, N, K, dtype, la, lb)
+    hA = torch.from_numpy(A.view(np.int16).ravel()).pin_memory()
+    hB = torch.from_numpy(Bm.view(np.int16).ravel()).pin_memory()
+    dA = torch.empty_like(hA, device="cuda")
+    dB = torch.empty_like(hB, device="cuda")
+    dC = torch.empty(M * N, dtype=torch.int16, device="cuda")
+    stream = torch.cuda.current_stream()
+    for sched, chunks, opts in (("persistent", 3, {}), ("dp", 4, {}), ("persistent", 16, {}),
+                                ("persistent", 1, {}), ("streamk", 3, {}),
+                                ("streamk", 4, {"sk_mode": 1}), ("splitk", 3, {})):
+        p = B.Plan(M, N, K, dtype, la, lb, sched, host_chunks=chunks, **opts)
+        tm = p.info("tile_m")
+        rows = -(-(-(-M // chunks)) // tm) * tm          # whole tiles per chunk
+        want = 1 if chunks == 1 else -(-M // rows)
+        assert p.info("host_chunks") in (want, 1), (sched, chunks)
+        if sched in ("persistent", "dp"):
+            assert p.info("host_chunks") == want
+        for _ in range(2):   # the second call reuses the pipeline
+            hC = torch.full((M * N,), 0x7E5A, dtype=torch.int16).pin_memory()
+            p.run_host(hA, hB, hC, dA, dB, dC, None if not p.workspace_size else
+                       torch.zeros(p.workspace_size, dtype=torch.uint8, device="cuda"), stream)
+            assert p.last_status(stream) == B.GEMM_OK
+            assert np.array_equal(hC.numpy().view(np.uint16).reshape(M, N), Cref), (sched, chunks)
+        p.close()
+
+
 def test_run_host_end_to_end():
     M, N, K, dtype = 256, 384, 640, inputs.BF16
     A, Bm = inputs.operands(M, N, K, dtype, 0, 1, ("normal", 1.0), ("normal", 1.0), 12)
