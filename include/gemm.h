@@ -145,8 +145,8 @@ enum {
      * Hilbert-curve scheduling).  The order is built on the host and copied
      * to a small device table owned by the plan when the option is set. */
     GEMM_OPT_RASTER = 13,
-    /* gemm_run_host: 0 (default) = pipelined in 4 row chunks when M >= 2048,
-     * else serial; 1 = always serial; 2..16 = that many row chunks (each a
+    /* gemm_run_host: 0 (default) = pipelined in min(8, M / 512) row chunks
+     * when M >= 2048, else serial; 1 = always serial; 2..16 = that many row chunks (each a
      * whole number of scheduled tile rows, so fewer may result).  Serial
      * whenever the chunks' sub-plans would need more workspace than
      * gemm_workspace_size of this plan.  GEMM_INFO_HOST_CHUNKS reports the

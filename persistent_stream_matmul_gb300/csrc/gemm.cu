@@ -585,7 +585,7 @@ int host_chunks(const gemm_plan* p, int64_t* rows_out) {
         if (p->opt_host_chunks >= 2)
             n = p->opt_host_chunks;
         else if (p->M >= 2048)
-            n = 4;
+            n = (int)std::min<int64_t>(8, p->M / 512);  // chunks of at least 512 rows
     }
     int64_t rows = p->M;
     if (n > 1) {

@@ -307,12 +307,13 @@ def test_host_chunk_policy(lib):
         rows = p.info("tile_m")
         p.close()
         return n, rows
-    assert chunks(8192, "persistent")[0] == 4
-    assert chunks(8192, "dp")[0] == 4
-    assert chunks(8192, "auto")[0] == 4          # AUTO resolves to persistent here
+    assert chunks(8192, "persistent")[0] == 8
+    assert chunks(8192, "dp")[0] == 8
+    assert chunks(8192, "auto")[0] == 8          # AUTO resolves to persistent here
+    assert chunks(2048, "persistent")[0] == 4    # min(8, M / 512)
     assert chunks(2047, "persistent")[0] == 1    # too few rows for the default
-    assert chunks(8192, "streamk")[0] == 4       # sub-plans fit the plan's workspace
-    assert chunks(8192, "splitk")[0] == 4
+    assert chunks(8192, "streamk")[0] == 8       # sub-plans fit the plan's workspace
+    assert chunks(8192, "splitk")[0] == 8
     assert chunks(8192, "persistent", host_chunks=1)[0] == 1
     # chunk rows round up to whole scheduled tiles: 1000 rows in 256-row tiles
     # -> 3 requested chunks of 512 rows become 2
