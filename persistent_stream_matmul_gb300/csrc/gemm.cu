@@ -632,16 +632,18 @@ void pipe_release(gemm_plan* p) {
     if (p->sub_full) gemm_plan_destroy(p->sub_full);
     if (p->sub_last) gemm_plan_destroy(p->sub_last);
     p->sub_full = p->sub_last = nullptr;
-    if (p->pipe_ready) {
-        cudaStreamDestroy(p->h2d);
-        cudaStreamDestroy(p->d2h);
-        cudaEventDestroy(p->ev_start);
-        cudaEventDestroy(p->ev_done);
-        for (int i = 0; i < 16; ++i) {
-            cudaEventDestroy(p->ev_a[i]);
-            cudaEventDestroy(p->ev_c[i]);
-        }
+    // every handle is null until created, so a partly made pipeline is freed too
+    if (p->h2d) cudaStreamDestroy(p->h2d);
+    if (p->d2h) cudaStreamDestroy(p->d2h);
+    if (p->ev_start) cudaEventDestroy(p->ev_start);
+    if (p->ev_done) cudaEventDestroy(p->ev_done);
+    for (int i = 0; i < 16; ++i) {
+        if (p->ev_a[i]) cudaEventDestroy(p->ev_a[i]);
+        if (p->ev_c[i]) cudaEventDestroy(p->ev_c[i]);
+        p->ev_a[i] = p->ev_c[i] = nullptr;
     }
+    p->h2d = p->d2h = nullptr;
+    p->ev_start = p->ev_done = nullptr;
     p->pipe_ready = false;
     p->sub_rows = 0;
 }
@@ -659,7 +661,8 @@ gemm_status_t pipe_prepare(gemm_plan* p, int64_t rows) {
              cudaEventCreateWithFlags(&p->ev_c[i], ev_flags) == cudaSuccess;
     if (!ok) {
         cudaGetLastError();
-        return GEMM_ERR_CUDA;  // the plan keeps pipe_ready = false; what was made leaks
+        pipe_release(p);
+        return GEMM_ERR_CUDA;
     }
     p->pipe_ready = true;
     p->sub_rows = rows;
@@ -988,6 +991,12 @@ gemm_status_t gemm_run_host(gemm_plan_t p, const void* hA, const void* hB, void*
         }
         PSM_CUDA(cudaEventRecord(p->ev_a[i], p->h2d));
     }
+    // The sub-plans and this plan share `workspace`, each with its own flag
+    // layout: the sub-plans clear their (small) flag region on every call,
+    // and this plan clears its own again on its next gemm_run.
+    p->sub_full->flags_cleared_for = nullptr;
+    if (p->sub_last) p->sub_last->flags_cleared_for = nullptr;
+    p->flags_cleared_for = nullptr;
     for (int i = 0; i < chunks; ++i) {
         const int64_t r0 = (int64_t)i * rows;
         gemm_plan* sp = (i == chunks - 1 && p->sub_last) ? p->sub_last : p->sub_full;

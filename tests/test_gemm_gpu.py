@@ -349,6 +349,35 @@ def test_run_host_pipelined_chunks(la, lb):
         p.close()
 
 
+def test_run_host_pipeline_follows_options_and_shares_the_workspace():
+    # a Stream-K plan: pipelined host runs, device runs and an option change in
+    # between, all on one workspace; every result exact
+    M, N, K, dtype = 2048, 768, 1024, inputs.F16
+    A, Bm = inputs.operands(M, N, K, dtype, 0, 0, inputs.INT_LAW, inputs.INT_LAW, 47)
+    _, _, Cref = oracle.gemm(A, Bm, M, N, K, dtype, 0, 0)
+    hA = torch.from_numpy(A.view(np.int16).ravel()).pin_memory()
+    hB = torch.from_numpy(Bm.view(np.int16).ravel()).pin_memory()
+    dA, dB = hA.cuda(), hB.cuda()
+    dC = torch.empty(M * N, dtype=torch.int16, device="cuda")
+    stream = torch.cuda.current_stream()
+    p = B.Plan(M, N, K, dtype, 0, 0, "streamk", sk_mode=1)
+    assert p.info("host_chunks") == 4 and p.workspace_size > 0
+    w = torch.zeros(p.workspace_size, dtype=torch.uint8, device="cuda")
+    for step in range(6):
+        if step == 3:
+            p.set_option(B.GEMM_OPT_HOST_CHUNKS, 3)   # the pipeline is rebuilt
+            assert p.info("host_chunks") in (2, 3)
+        hC = torch.full((M * N,), 0x7E5A, dtype=torch.int16).pin_memory()
+        p.run_host(hA, hB, hC, dA, dB, dC, w, stream)
+        assert p.last_status(stream) == B.GEMM_OK
+        assert np.array_equal(hC.numpy().view(np.uint16).reshape(M, N), Cref), step
+        dC.fill_(0x7E5A)
+        p.run(dA, dB, dC, w, stream)
+        assert p.last_status(stream) == B.GEMM_OK
+        assert np.array_equal(dC.cpu().numpy().view(np.uint16).reshape(M, N), Cref), step
+    p.close()
+
+
 def test_run_host_end_to_end():
     M, N, K, dtype = 256, 384, 640, inputs.BF16
     A, Bm = inputs.operands(M, N, K, dtype, 0, 1, ("normal", 1.0), ("normal", 1.0), 12)
