@@ -5,10 +5,15 @@
 //
 // Clusters (CM = 2): the two CTAs of a cluster run the same scheduled unit on
 // the two 128-row halves of a 256-row tile, so they need the same B tile.
-// Each CTA loads its own A and half of B, multicasting that half into both
-// CTAs' rings; a stage's empty barrier counts the MMA commits of both CTAs, so
-// neither refills a stage the other is still reading.  L2-to-SM traffic per
-// CTA drops from A + B to A + B/2 per k-slice.
+// Each CTA loads its own A and half of B; L2-to-SM traffic per CTA drops from
+// A + B to A + B/2 per k-slice.  Two ways to use the halves:
+//   PAIR_MMA   one thread of the first CTA issues tcgen05.mma.cta_group::2
+//              (256 x BN) over both CTAs' shared memory, each CTA keeping only
+//              its half of B (a deeper ring); both CTAs' copies complete on the
+//              first CTA's barriers, and one multicast commit frees both rings.
+//   otherwise  each CTA multicasts its half of B into both rings and runs its
+//              own 128 x BN MMA; a stage's empty barrier counts the commits of
+//              both CTAs, so neither refills a stage the other still reads.
 //
 // Warp roles (192 threads, one CTA per SM):
 //   warp 0      TMA producer: one lane fills a STAGES-deep ring of A/B tiles
@@ -24,7 +29,9 @@
 //               to this CTA's workspace slot, then post the tile's flag.
 //               OWNER unit (holds k-iteration 0): wait until all the tile's
 //               peers have posted, add their partials in ascending k, round
-//               once, store C.
+//               once, store C.  At a CTA's last unit the ring is idle: the
+//               peers' partials are copied into it in one round trip, and C
+//               is staged there and written as whole rows.
 //
 // Sources: the HF post "naive vs persistent matmul" (tile per thread-block,
 // persistent thread-blocks, warp specialisation and double buffering named
@@ -75,8 +82,7 @@ struct Cfg {
     static constexpr int STAGES = STAGES_FIT > 12 ? 12 : STAGES_FIT;
     static constexpr int TMEM_COLS = 2 * BN;  // two accumulators; 256 or 512
     static constexpr int BAR_BYTES = 256;
-    static constexpr int SLACK_BYTES = 0;
-    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + SLACK_BYTES + BAR_BYTES + 1024;
+    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + BAR_BYTES + 1024;
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
     static_assert(BN == 64 || BN == 128 || BN == 256, "tile width");
     static_assert(AROWS == 128 || AROWS == 64, "rows of A per stage");
@@ -180,8 +186,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
     const uint32_t sbase = raw + pad;
-    uint8_t* bar_area = smem_raw + pad + STAGES * Cf::STAGE_BYTES + Cf::SLACK_BYTES;
-    const uint32_t bar_base = sbase + STAGES * Cf::STAGE_BYTES + Cf::SLACK_BYTES;
+    uint8_t* bar_area = smem_raw + pad + STAGES * Cf::STAGE_BYTES;
+    const uint32_t bar_base = sbase + STAGES * Cf::STAGE_BYTES;
     auto full_bar = [&](int s) { return bar_base + 8u * s; };
     auto empty_bar = [&](int s) { return bar_base + 8u * (STAGES + s); };
     auto tfull_bar = [&](int b) { return bar_base + 8u * (2 * STAGES + b); };
