@@ -27,10 +27,11 @@
  *   GEMM_SCHED_AUTO           the plan picks one of the above from the shape
  *                             (GEMM_INFO_SCHEDULE and GEMM_INFO_SK_MODE report
  *                             which): Stream-K for a single row of tiles;
- *                             persistent for tiny problems, for four or more
- *                             waves of tiles and for nearly one full wave;
- *                             Stream-K (hybrid, or all tiles when the hybrid
- *                             would split a few tiles many ways) otherwise.
+ *                             persistent for tiny problems, for nearly one
+ *                             full wave, and for 4+ waves of short tiles
+ *                             (< 64 k-iterations, < 12 waves); Stream-K
+ *                             (hybrid, or all tiles when the hybrid would
+ *                             split a few tiles many ways) otherwise.
  *
  * Conventions for every entry point:
  *  - Each call returns a gemm_status_t; nothing else crosses the ABI.  An

@@ -236,8 +236,10 @@ gemm_status_t derive(gemm_plan* p) {
     //  * one row of tiles (skinny, memory-bound) -> Stream-K, whose units
     //    start at different k and so spread the B stream;
     //  * fewer than 8 k-iterations per unit -> persistent (nothing to split);
-    //  * four or more waves of tiles -> persistent (the tail is at most a
-    //    quarter wave, and whole tiles keep the grouped raster's L2 reuse);
+    //  * four or more waves of tiles -> the hybrid rule, which removes the
+    //    last partial wave, when tiles have at least 64 k-iterations or there
+    //    are at least 12 waves; else persistent (few waves of short tiles put
+    //    a large share of the work in short split units);
     //  * under one wave -> Stream-K when at most 70% of the units would have
     //    a tile, else persistent (the fixup costs more than the idle units);
     //  * one to four waves -> the hybrid rule when each split tile has at most
@@ -252,8 +254,11 @@ gemm_status_t derive(gemm_plan* p) {
         if (tiles - sk_h > g) sk_h += g;
         if (tiles_m == 1 && tiles < g) {
             sched = GEMM_SCHED_STREAMK;
-        } else if (tiles * ipt < 8 * (int64_t)g || waves >= 4.0) {
+        } else if (tiles * ipt < 8 * (int64_t)g) {
             sched = GEMM_SCHED_PERSISTENT;
+        } else if (waves >= 4.0) {
+            sched = (ipt >= 64 || waves >= 12.0) ? GEMM_SCHED_STREAMK : GEMM_SCHED_PERSISTENT;
+            sk_mode = 0;
         } else if (waves < 1.0) {
             sched = (tiles * 10 <= 7 * (int64_t)g) ? GEMM_SCHED_STREAMK : GEMM_SCHED_PERSISTENT;
         } else {

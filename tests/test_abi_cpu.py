@@ -158,9 +158,9 @@ def test_splitk_units(lib, M, N, K, cm):
 def test_auto_schedule_choices(lib):
     cases = {  # workload -> (schedule, all tiles in the Stream-K wave)
         (512, 512, 512): (B.GEMM_SCHED_PERSISTENT, 0),
-        (8192, 8192, 8192): (B.GEMM_SCHED_PERSISTENT, 0),
+        (8192, 8192, 8192): (B.GEMM_SCHED_STREAMK, 0),
         (2304, 2304, 8192): (B.GEMM_SCHED_STREAMK, 1),
-        (8192, 14336, 4096): (B.GEMM_SCHED_PERSISTENT, 0),
+        (8192, 14336, 4096): (B.GEMM_SCHED_STREAMK, 0),
         (64, 8192, 8192): (B.GEMM_SCHED_STREAMK, 1),
         # from the timed sweep of log-sampled shapes
         (3840, 2816, 5888): (B.GEMM_SCHED_STREAMK, 0),
@@ -169,6 +169,10 @@ def test_auto_schedule_choices(lib):
         (256, 1792, 6400): (B.GEMM_SCHED_STREAMK, 1),
         (512, 5632, 1280): (B.GEMM_SCHED_STREAMK, 1),
         (4608, 5120, 1024): (B.GEMM_SCHED_PERSISTENT, 0),
+        # four or more waves: hybrid for long tiles or many waves
+        (5120, 5120, 5120): (B.GEMM_SCHED_STREAMK, 0),
+        (4096, 8192, 2048): (B.GEMM_SCHED_PERSISTENT, 0),
+        (12288, 12288, 2048): (B.GEMM_SCHED_STREAMK, 0),
     }
     for (M, N, K), (sched, mode) in cases.items():
         p = B.Plan(M, N, K, B.GEMM_BF16, 0, 1, "auto", offline_sms=152)
@@ -309,7 +313,7 @@ def test_host_chunk_policy(lib):
         return n, rows
     assert chunks(8192, "persistent")[0] == 8
     assert chunks(8192, "dp")[0] == 8
-    assert chunks(8192, "auto")[0] == 8          # AUTO resolves to persistent here
+    assert chunks(8192, "auto")[0] == 8          # AUTO resolves to hybrid Stream-K here
     assert chunks(2048, "persistent")[0] == 4    # min(8, M / 512)
     assert chunks(2047, "persistent")[0] == 1    # too few rows for the default
     assert chunks(8192, "streamk")[0] == 8       # sub-plans fit the plan's workspace
