@@ -330,23 +330,33 @@ def main():
     sampler = ClockSampler(device_pci_id(torch, local_rank))
     sampler.start()
 
-    # per-schedule device time (each launch bracketed by events on this stream)
+    # per-schedule device time (each launch bracketed by events on this stream),
+    # in interleaved rounds so that every schedule samples the same drift of
+    # the clocks under the power cap
     per_sched = {}
-    for s in (SCHED_NAMES if args.schedule == "best" else [args.schedule]):
+    names = SCHED_NAMES if args.schedule == "best" else [args.schedule]
+    rounds = 3
+    per_round = max(1, -(-args.steps // rounds))
+    times = {s: [] for s in names}
+    for rnd in range(rounds):
+        for s in names:
+            p, w = plans[s], wss[s]
+            for i in range(args.warmup if rnd == 0 else 1):
+                p.run(*sets[i % copies], w, stream)
+            torch.cuda.synchronize()
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * per_round)]
+            for i in range(per_round):
+                ev[2 * i].record(stream)
+                p.run(*sets[(args.warmup + i) % copies], w, stream)
+                ev[2 * i + 1].record(stream)
+            torch.cuda.synchronize()
+            st = p.last_status(stream)
+            if st != B.GEMM_OK:
+                raise RuntimeError("device status after %s: %s" % (s, B.gemm_status_string(st)))
+            times[s] += [ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(per_round)]
+    for s in names:
         p, w = plans[s], wss[s]
-        for i in range(args.warmup):
-            p.run(*sets[i % copies], w, stream)
-        torch.cuda.synchronize()
-        ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * args.steps)]
-        for i in range(args.steps):
-            ev[2 * i].record(stream)
-            p.run(*sets[(args.warmup + i) % copies], w, stream)
-            ev[2 * i + 1].record(stream)
-        torch.cuda.synchronize()
-        st = p.last_status(stream)
-        if st != B.GEMM_OK:
-            raise RuntimeError("device status after %s: %s" % (s, B.gemm_status_string(st)))
-        ms = [ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(args.steps)]
+        ms = times[s]
         med = statistics.median(ms)
         per_sched[s] = {"tflops": flops / (med * 1e-3) / 1e12, "ms_median": med,
                         "ms_min": min(ms), "ms_max": max(ms)}
