@@ -250,7 +250,8 @@ gemm_status_t gemm_run(gemm_plan_t plan, const void *A, const void *B, void *C,
  *    wait for the last copy out, so everything enqueued on `stream` before
  *    the call precedes it and everything after it follows it.  The first
  *    pipelined call of a plan creates the two streams, the events and two
- *    internal sub-plans (released by gemm_plan_destroy or an option change);
+ *    internal sub-plans (released by gemm_plan_destroy or an option change;
+ *    if they cannot be made, the call runs the serial path instead);
  *    the chunks run one after another on `stream` and share `workspace`.
  * Errors: as gemm_run; CUDA when a copy, stream or event call fails.
  */

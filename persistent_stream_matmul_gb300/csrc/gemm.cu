@@ -954,7 +954,10 @@ gemm_status_t gemm_run_host(gemm_plan_t p, const void* hA, const void* hB, void*
     const size_t a_bytes = (size_t)p->M * p->K * 2, b_bytes = (size_t)p->K * p->N * 2;
     const size_t c_bytes = (size_t)p->M * p->N * 2;
     int64_t rows = 0;
-    const int chunks = host_chunks(p, &rows);
+    int chunks = host_chunks(p, &rows);
+    // the pipeline is a speed-up only: if its streams, events or sub-plans
+    // cannot be made, run the serial path
+    if (chunks > 1 && pipe_prepare(p, rows) != GEMM_OK) chunks = 1;
     if (chunks <= 1) {
         if (p->K > 0) {
             if (cudaMemcpyAsync(dA, hA, a_bytes, cudaMemcpyHostToDevice, st) != cudaSuccess ||
@@ -971,8 +974,6 @@ gemm_status_t gemm_run_host(gemm_plan_t p, const void* hA, const void* hB, void*
     // C computed (caller's stream) -> chunk i of C out (second copy stream),
     // so the three overlap across chunks.  Entry and exit are ordered with
     // the caller's stream through events.
-    gemm_status_t ps = pipe_prepare(p, rows);
-    if (ps != GEMM_OK) return ps;
     const bool a_col = p->layout_a == GEMM_COL_MAJOR;
     const char* ha = static_cast<const char*>(hA);
     char* da = static_cast<char*>(dA);
