@@ -50,3 +50,33 @@ def test_single_rank_and_busy_fraction():
     st = np.array([[0, 1, 5, 100], [0, 1, 5, 50]], dtype=np.int64)
     r = bench.sm_busy_fraction(st, 2)
     assert abs(r["sm_busy_frac"] - 0.75) < 1e-12 and r["span_us"] == 0.1
+
+
+def _bench(args, env_extra):
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ)
+    env.update(env_extra)
+    out = subprocess.run([sys.executable, os.path.join(root, "bench.py")] + args, cwd=root, env=env,
+                         capture_output=True, text=True, timeout=600)
+    assert out.returncode == 0, out.stderr[-2000:]
+    lines = [l for l in out.stdout.splitlines() if l.startswith("{")]
+    return [json.loads(l) for l in lines]
+
+
+def test_reference_arm_line_on_rank_zero_only():
+    """bench.py --impl reference times the CPU oracle on the host; rank 0 prints
+    the contract's line, any other rank exits 0 without work."""
+    args = ["--impl", "reference", "--steps", "2", "--warmup", "3", "--workload", "square512_f16",
+            "--reference-rows", "8"]
+    lines = _bench(args, {"RANK": "0", "WORLD_SIZE": "1"})
+    assert len(lines) == 1
+    d = lines[0]
+    assert d["impl"] == "reference" and d["value"] > 0 and d["unit"] == "TFLOP/s"
+    assert d["steps"] == 2 and d["warmup"] == 3 and d["higher_is_better"] is True
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
+    assert d["config"]["workload"] == "square512_f16"
+    assert _bench(args, {"RANK": "1", "WORLD_SIZE": "2"}) == []
