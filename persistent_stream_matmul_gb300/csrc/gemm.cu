@@ -165,8 +165,10 @@ void* pick_kernel(int BN, int dtype, int CM, int AROWS = 128, int PAIR = 0) {
         if (AROWS == 64) return bf ? kernel_ptr<64, true, 1, 64>() : kernel_ptr<64, false, 1, 64>();
         return bf ? kernel_ptr<64, true, 1>() : kernel_ptr<64, false, 1>();
     }
-    if (AROWS == 64)  // BN = 128, CM = 1
+    if (AROWS == 64) {  // BN = 128 or 256, CM = 1
+        if (BN == 256) return bf ? kernel_ptr<256, true, 1, 64>() : kernel_ptr<256, false, 1, 64>();
         return bf ? kernel_ptr<128, true, 1, 64>() : kernel_ptr<128, false, 1, 64>();
+    }
     return CM == 2 ? pick_kernel_cm<2>(BN, dtype) : pick_kernel_cm<1>(BN, dtype);
 }
 
@@ -174,7 +176,7 @@ int kernel_index(int BN, int dtype, int CM, int AROWS, int PAIR) {
     const int bf = dtype == GEMM_BF16 ? 1 : 0;
     if (PAIR) return 14 + 4 * (AROWS == 64 ? 1 : 0) + 2 * (BN == 256 ? 1 : 0) + bf;
     if (BN == 64) return 10 + 2 * (AROWS == 64 ? 1 : 0) + bf;
-    if (AROWS == 64) return 8 + bf;
+    if (AROWS == 64) return (BN == 256 ? 22 : 8) + bf;
     return (BN == 256 ? 4 : 0) + 2 * bf + (CM == 2 ? 1 : 0);
 }
 
@@ -183,14 +185,14 @@ int smem_for(int BN, int AROWS = 128, int PAIR = 0) {
         return BN == 256 ? Cfg<256, 64, true>::SMEM_BYTES : Cfg<128, 64, true>::SMEM_BYTES;
     if (PAIR) return BN == 256 ? Cfg<256, 128, true>::SMEM_BYTES : Cfg<128, 128, true>::SMEM_BYTES;
     if (BN == 64) return AROWS == 64 ? Cfg<64, 64>::SMEM_BYTES : Cfg<64>::SMEM_BYTES;
-    if (AROWS == 64) return Cfg<128, 64>::SMEM_BYTES;
+    if (AROWS == 64) return BN == 256 ? Cfg<256, 64>::SMEM_BYTES : Cfg<128, 64>::SMEM_BYTES;
     return BN == 256 ? Cfg<256>::SMEM_BYTES : Cfg<128>::SMEM_BYTES;
 }
 int stages_for(int BN, int AROWS = 128, int PAIR = 0) {
     if (PAIR && AROWS == 64) return BN == 256 ? Cfg<256, 64, true>::STAGES : Cfg<128, 64, true>::STAGES;
     if (PAIR) return BN == 256 ? Cfg<256, 128, true>::STAGES : Cfg<128, 128, true>::STAGES;
     if (BN == 64) return AROWS == 64 ? Cfg<64, 64>::STAGES : Cfg<64>::STAGES;
-    if (AROWS == 64) return Cfg<128, 64>::STAGES;
+    if (AROWS == 64) return BN == 256 ? Cfg<256, 64>::STAGES : Cfg<128, 64>::STAGES;
     return BN == 256 ? Cfg<256>::STAGES : Cfg<128>::STAGES;
 }
 
@@ -345,8 +347,8 @@ gemm_status_t derive(gemm_plan* p) {
     // only its half of B, so the ring is deeper
     p->PAIR = (CM == 2 && p->opt_pair_mma == 1) ? 1 : 0;
     // at most 64 valid rows: load only 64 rows of A per stage (without
-    // clusters for tiles up to 128 wide, or with a pair MMA)
-    p->AROWS = (p->M <= 64 && ((CM == 1 && BN <= 128) || p->PAIR)) ? 64 : 128;
+    // clusters, or with a pair MMA)
+    p->AROWS = (p->M <= 64 && (CM == 1 || p->PAIR)) ? 64 : 128;
     p->ctas = s.grid * CM;
     p->stages = stages_for(BN, p->AROWS, p->PAIR);
     p->smem_bytes = smem_for(BN, p->AROWS, p->PAIR);

@@ -77,7 +77,7 @@ struct Cfg {
     static constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
     // ring of up to 224 KB (the CTA may hold 227 KB; barriers and alignment
     // take the rest): 4 stages at BN=256, 7 at BN=128 or with a pair MMA at
-    // BN=256, 9 with half-height A at BN=128, at most 12
+    // BN=256, 9 with half-height A at BN=128, 5 with it at BN=256, at most 12
     static constexpr int STAGES_FIT = (224 * 1024) / STAGE_BYTES;
     static constexpr int STAGES = STAGES_FIT > 12 ? 12 : STAGES_FIT;
     static constexpr int TMEM_COLS = 2 * BN;  // two accumulators; 256 or 512
@@ -530,11 +530,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 constexpr uint32_t PEER_STAGE_BYTES = (uint32_t)BN * SROWS * 4;
                 constexpr uint32_t RING_BYTES = (uint32_t)STAGES * Cf::STAGE_BYTES;
                 static_assert(C_STAGE_BYTES <= RING_BYTES, "C tile fits the ring");
-                const uint32_t pstage = sbase + C_STAGE_BYTES;
+                // All peers beside the C tile when they fit; else all peers with C
+                // stored straight from registers; else as many as fit beside C.
+                bool c_staged = last;
                 int staged = 0;
-                if (last) fence_proxy_async_smem();  // the ring was last used by the async proxy
                 if (last && u.role == ROLE_OWNER && store) {
-                    staged = min(u.npeers, (int)((RING_BYTES - C_STAGE_BYTES) / PEER_STAGE_BYTES));
+                    const uint32_t all_peers = (uint32_t)u.npeers * PEER_STAGE_BYTES;
+                    if (C_STAGE_BYTES + all_peers > RING_BYTES && all_peers <= RING_BYTES)
+                        c_staged = false;
+                    staged = c_staged
+                                 ? min(u.npeers, (int)((RING_BYTES - C_STAGE_BYTES) / PEER_STAGE_BYTES))
+                                 : u.npeers;
+                }
+                const uint32_t pstage = sbase + (c_staged ? C_STAGE_BYTES : 0u);
+                if (last) fence_proxy_async_smem();  // the ring was last used by the async proxy
+                if (staged > 0) {
                     if (row_ok && staged > 0) {
                         const float4* part = reinterpret_cast<const float4*>(p.partials);
                         const size_t slot_f4 = (size_t)BM * BN / 4;
@@ -613,7 +623,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         }
                     }
                     if (store && row_ok) {
-                        if (last) {
+                        if (c_staged) {
                             const uint32_t srow = sbase + (uint32_t)(row_in_tile * BN * 2);
 #pragma unroll
                             for (int v = 0; v < 4; ++v) {
@@ -646,7 +656,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     else
                         mbar_arrive(tempty_bar(buf));
                 }
-                if (last && store) {
+                if (c_staged && store) {
                     // every epilogue warp has staged its rows; write whole rows:
                     // lane l takes unit l % C_UNITS of row i * (32 / C_UNITS) + l / C_UNITS
                     named_bar_sync(BAR_EPI_SYNC, EPI_THREADS);

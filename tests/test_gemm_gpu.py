@@ -140,6 +140,26 @@ def test_all_streamk_mode_and_short_m(dtype):
 
 
 @pytest.mark.parametrize("dtype", [inputs.F16, inputs.BF16])
+def test_owner_stages_all_peers_when_c_does_not_fit_beside_them(dtype):
+    # 64 rows, 256-wide tiles, four contributors per tile: the owner's three
+    # peer partials fill the 200 KB ring, so C is stored straight from registers
+    M, N, K = 64, 1024, 2048
+    ws = Workspace()
+    for la, lb in ((0, 0), (0, 1)):
+        A, Bm, dA, dB = _case(M, N, K, dtype, la, lb, inputs.INT_LAW, 48)
+        _, _, Cref = oracle.gemm(A, Bm, M, N, K, dtype, la, lb)
+        for g in (16, 12, 20):
+            p = B.Plan(M, N, K, dtype, la, lb, "streamk", tile_n=256, cluster_m=1, grid=g)
+            assert p.info("a_rows_per_stage") == 64 and p.info("tiles") == 4
+            npeers = max(u[4] for c in range(g) for u in p.units(c))
+            assert npeers >= 3 or g != 16
+            got = run(p, dA, dB, M, N, ws)
+            assert np.array_equal(got, Cref), (la, lb, g)
+            assert np.array_equal(run(p, dA, dB, M, N, ws), got)
+            p.close()
+
+
+@pytest.mark.parametrize("dtype", [inputs.F16, inputs.BF16])
 def test_splitk_parts_integer_exact(dtype):
     ws = Workspace()
     for (M, N, K), la, lb in (((384, 1024, 2048), 0, 1), ((64, 2048, 3000 // 8 * 8), 0, 0),
