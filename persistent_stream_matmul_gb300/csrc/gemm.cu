@@ -558,7 +558,9 @@ void sub_options(const gemm_plan* p, gemm_plan* sp) {
     sp->opt_two_tiles = p->opt_two_tiles;
     sp->opt_cluster_m = p->CM;
     sp->opt_sk_mode = p->opt_sk_mode;
-    sp->opt_split = p->opt_split;
+    // split-K: the parent's resolved part count, so every chunk sums in the
+    // parent's order (and a parent without partials gets sub-plans without)
+    sp->opt_split = p->eff_schedule == GEMM_SCHED_SPLITK ? p->s.split : p->opt_split;
     sp->opt_k_rotate = p->opt_k_rotate;
     sp->opt_l2_prefetch = p->opt_l2_prefetch;
     sp->opt_pair_mma = p->opt_pair_mma;
@@ -601,7 +603,7 @@ int host_chunks(const gemm_plan* p, int64_t* rows_out) {
         rows = (rows + unit - 1) / unit * unit;
         n = (int)((p->M + rows - 1) / rows);
     }
-    if (n > 1 && p->ws_bytes > 0) {
+    if (n > 1) {
         size_t f1 = 0, q1 = 0, f2 = 0, q2 = 0;
         bool ok = sub_workspace(p, rows, &f1, &q1);
         if (ok && p->M % rows) ok = sub_workspace(p, p->M % rows, &f2, &q2);

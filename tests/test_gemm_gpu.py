@@ -369,6 +369,27 @@ def test_run_host_pipelined_chunks(la, lb):
         p.close()
 
 
+def test_run_host_splitk_chunks_keep_the_parents_part_count():
+    # a split-K plan with one part per tile needs no workspace; its row-chunk
+    # sub-plans keep that part count (found by a randomized parity sweep: they
+    # used to pick more parts and ask for a workspace the caller never sized)
+    M, N, K, dtype = 1000, 592, 2368, inputs.BF16
+    A, Bm = inputs.operands(M, N, K, dtype, 0, 0, inputs.INT_LAW, inputs.INT_LAW, 49)
+    _, _, Cref = oracle.gemm(A, Bm, M, N, K, dtype, 0, 0)
+    hA = torch.from_numpy(A.view(np.int16).ravel()).pin_memory()
+    hB = torch.from_numpy(Bm.view(np.int16).ravel()).pin_memory()
+    dA, dB = hA.cuda(), hB.cuda()
+    dC = torch.empty(M * N, dtype=torch.int16, device="cuda")
+    stream = torch.cuda.current_stream()
+    p = B.Plan(M, N, K, dtype, 0, 0, "splitk", group_m=1, host_chunks=2)
+    assert p.info("split_k") == 1 and p.workspace_size == 0 and p.info("host_chunks") == 2
+    hC = torch.full((M * N,), 0x7E5A, dtype=torch.int16).pin_memory()
+    p.run_host(hA, hB, hC, dA, dB, dC, None, stream)
+    assert p.last_status(stream) == B.GEMM_OK
+    assert np.array_equal(hC.numpy().view(np.uint16).reshape(M, N), Cref)
+    p.close()
+
+
 def test_run_host_pipeline_follows_options_and_shares_the_workspace():
     # a Stream-K plan: pipelined host runs, device runs and an option change in
     # between, all on one workspace; every result exact
