@@ -9,7 +9,9 @@
 * ``shape_sweep``: the same issue's shape sampler: M, N and K drawn from
   multiples of 256 spaced evenly in log2 between 256 and 8192, a fixed random
   sample of the triples (seed 123); each shape timed with every schedule and
-  with GEMM_SCHED_AUTO.
+  with GEMM_SCHED_AUTO.  ``--large`` adds ``LARGE_SHAPES``, products of four or
+  more waves of tiles that the sampler rarely draws under its size cap; the
+  rule for that regime in GEMM_SCHED_AUTO was fitted on them.
 
 Run as ``python -m persistent_stream_matmul_gb300.tune --help``.  Operands
 are random device data (timing does not depend on the values); correctness
@@ -33,6 +35,13 @@ SCHEDULE_VARIANTS = {
     "splitk": ("splitk", {}),
     "auto": ("auto", {}),
 }
+
+
+# four or more waves of 256 x 256 tiles on 76 SM pairs, short and long k
+LARGE_SHAPES = [(8192, 8192, 8192), (8192, 14336, 4096), (4096, 4096, 4096), (16384, 4096, 4096),
+                (6144, 6144, 6144), (8192, 4096, 8192), (4096, 14336, 4096), (2048, 8192, 8192),
+                (3072, 3072, 8192), (12288, 12288, 2048), (4096, 8192, 2048), (8192, 8192, 1024),
+                (5120, 5120, 5120), (2560, 10240, 4096)]
 
 
 def log_sampled_values(lo: int = 256, hi: int = 8192, step: int = 256, n: int = 1000):
@@ -122,12 +131,12 @@ def grid_sweep(M, N, K, dtype=B.GEMM_BF16, la=0, lb=1, seed=123, torch_mod=None)
 
 
 def shape_sweep(count, dtype=B.GEMM_BF16, la=0, lb=1, seed=123, max_macs=2.0 ** 36,
-                variants=None, torch_mod=None):
+                variants=None, torch_mod=None, extra_shapes=()):
     import torch as t
     t = torch_mod or t
     variants = variants or list(SCHEDULE_VARIANTS)
     rows = []
-    for (M, N, K) in sample_shapes(count, seed, max_macs):
+    for (M, N, K) in list(sample_shapes(count, seed, max_macs)) + list(extra_shapes):
         ops = Operands(M, N, K, t)
         res = {}
         for name in variants:
@@ -163,14 +172,16 @@ def main():
     ap.add_argument("--shapes", type=int, default=0, help="log-sampled shapes to time")
     ap.add_argument("--max-macs", type=float, default=2.0 ** 36)
     ap.add_argument("--dtype", choices=["bf16", "fp16"], default="bf16")
+    ap.add_argument("--large", action="store_true", help="also time LARGE_SHAPES")
     args = ap.parse_args()
     dtype = B.GEMM_BF16 if args.dtype == "bf16" else B.GEMM_F16
     B.load()
     if args.grid_sweep:
         for row in grid_sweep(*args.grid_sweep, dtype=dtype):
             print(json.dumps(row), flush=True)
-    if args.shapes:
-        rows = shape_sweep(args.shapes, dtype=dtype, max_macs=args.max_macs)
+    if args.shapes or args.large:
+        rows = shape_sweep(args.shapes, dtype=dtype, max_macs=args.max_macs,
+                           extra_shapes=LARGE_SHAPES if args.large else ())
         for row in rows:
             print(json.dumps(row), flush=True)
         print(json.dumps({"summary": summarize_shapes(rows)}), flush=True)
