@@ -13,6 +13,11 @@
   more waves of tiles that the sampler rarely draws under its size cap; the
   rule for that regime in GEMM_SCHED_AUTO was fitted on them.
 
+* ``paired_compare``: two option sets (or schedules) on one shape, timed in
+  short bursts that alternate between them (the order flips every pair), so
+  both see the same drift of the clocks under the power cap; reports the
+  median ratio and how many pairs each side won.
+
 Run as ``python -m persistent_stream_matmul_gb300.tune --help``.  Operands
 are random device data (timing does not depend on the values); correctness
 over sampled shapes is checked by the test suite, not here.
@@ -112,6 +117,53 @@ def time_plan(ops: Operands, dtype, la, lb, schedule, options, warmup=3, iters=1
         p.close()
 
 
+def burst_us(ops: Operands, dtype, la, lb, schedule, options, launches):
+    """Mean device time (us) of `launches` back-to-back runs of one plan."""
+    t = ops.t
+    p = B.Plan(ops.M, ops.N, ops.K, dtype, la, lb, schedule, **options)
+    try:
+        w = ops.workspace(p.workspace_size)
+        stream = t.cuda.current_stream()
+        for _ in range(3):
+            p.run(ops.a, ops.b, ops.c, w, stream)
+        e0, e1 = t.cuda.Event(enable_timing=True), t.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(launches):
+            p.run(ops.a, ops.b, ops.c, w, stream)
+        e1.record(stream)
+        t.cuda.synchronize()
+        if p.last_status(stream) != B.GEMM_OK:
+            raise B.GemmError(p.last_status(stream), "paired_compare")
+        return e0.elapsed_time(e1) / launches * 1e3
+    finally:
+        p.close()
+
+
+def paired_compare(M, N, K, base, variant, dtype=B.GEMM_BF16, la=0, lb=1, pairs=10,
+                   burst_ms=20.0, torch_mod=None):
+    """`base` and `variant` are dicts of plan options plus an optional
+    "schedule" (default "streamk"); returns medians and the paired ratio."""
+    import torch as t
+    t = torch_mod or t
+    ops = Operands(M, N, K, t)
+    sides = {"base": dict(base), "variant": dict(variant)}
+    scheds = {k: v.pop("schedule", "streamk") for k, v in sides.items()}
+    # launches per burst from one timing of the base
+    one = burst_us(ops, dtype, la, lb, scheds["base"], sides["base"], 3)
+    launches = max(5, int(burst_ms * 1e3 / max(one, 1.0)))
+    times = {"base": [], "variant": []}
+    for i in range(pairs):
+        order = ("base", "variant") if i % 2 == 0 else ("variant", "base")
+        for side in order:
+            times[side].append(burst_us(ops, dtype, la, lb, scheds[side], sides[side], launches))
+    ratios = [v / b for b, v in zip(times["base"], times["variant"])]
+    return {"M": M, "N": N, "K": K, "base": base, "variant": variant, "launches": launches,
+            "base_us": statistics.median(times["base"]),
+            "variant_us": statistics.median(times["variant"]),
+            "variant_over_base_pct": 100.0 * (statistics.median(ratios) - 1.0),
+            "variant_faster_pairs": sum(1 for r in ratios if r < 1.0), "pairs": pairs}
+
+
 def grid_sweep(M, N, K, dtype=B.GEMM_BF16, la=0, lb=1, seed=123, torch_mod=None):
     import torch as t
     t = torch_mod or t
@@ -173,9 +225,17 @@ def main():
     ap.add_argument("--max-macs", type=float, default=2.0 ** 36)
     ap.add_argument("--dtype", choices=["bf16", "fp16"], default="bf16")
     ap.add_argument("--large", action="store_true", help="also time LARGE_SHAPES")
+    ap.add_argument("--compare", nargs=5, metavar=("M", "N", "K", "BASE", "VARIANT"),
+                    help="paired bursts; BASE and VARIANT are JSON option dicts, e.g. "
+                         "'{\"schedule\": \"persistent\"}' '{\"schedule\": \"streamk\"}'")
+    ap.add_argument("--layout-b", type=int, default=1, help="0 row-major, 1 column-major B")
     args = ap.parse_args()
     dtype = B.GEMM_BF16 if args.dtype == "bf16" else B.GEMM_F16
     B.load()
+    if args.compare:
+        M, N, K = (int(x) for x in args.compare[:3])
+        print(json.dumps(paired_compare(M, N, K, json.loads(args.compare[3]), json.loads(args.compare[4]),
+                                        dtype=dtype, lb=args.layout_b)), flush=True)
     if args.grid_sweep:
         for row in grid_sweep(*args.grid_sweep, dtype=dtype):
             print(json.dumps(row), flush=True)

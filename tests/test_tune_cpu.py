@@ -27,3 +27,27 @@ def test_summary_ratios():
     s = tune.summarize_shapes(rows)
     assert math.isclose(s["x"]["geomean_vs_best"], math.sqrt(1.0 * 0.25))
     assert s["x"]["wins"] == 1 and s["y"]["wins"] == 1
+
+
+def test_paired_compare_alternates_and_reports_the_paired_ratio(monkeypatch):
+    calls = []
+
+    class FakeOps:
+        def __init__(self, M, N, K, torch_mod):
+            self.M, self.N, self.K = M, N, K
+
+    def fake_burst(ops, dtype, la, lb, schedule, options, launches):
+        calls.append((schedule, dict(options), launches))
+        return 90.0 if schedule == "streamk" else 100.0     # the variant is 10 % faster
+
+    monkeypatch.setattr(tune, "Operands", FakeOps)
+    monkeypatch.setattr(tune, "burst_us", fake_burst)
+    r = tune.paired_compare(8192, 8192, 8192, {"schedule": "persistent", "group_m": 8},
+                            {"schedule": "streamk"}, pairs=4, torch_mod=object())
+    assert math.isclose(r["variant_over_base_pct"], -10.0)
+    assert r["variant_faster_pairs"] == 4 and r["pairs"] == 4
+    assert r["base"] == {"schedule": "persistent", "group_m": 8}   # the caller's dicts are untouched
+    timed = [c[0] for c in calls[1:]]                               # after the sizing burst
+    assert timed == ["persistent", "streamk", "streamk", "persistent"] * 2
+    assert all(c[1] == {"group_m": 8} for c in calls if c[0] == "persistent")
+    assert r["launches"] == int(20.0 * 1e3 / 100.0)
