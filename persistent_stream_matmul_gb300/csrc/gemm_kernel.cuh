@@ -496,7 +496,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     else
                         mbar_arrive(tempty_bar(buf));
                 }
-                __threadfence();
+                // The barrier orders every epilogue thread's partial stores
+                // before thread 0's post, and the post is a release at GPU
+                // scope: an owner that acquires the flag sees all of them.
                 named_bar_sync(BAR_EPI_SYNC, EPI_THREADS);
                 if (et == 0 && cta != p.inject_skip_cta) post_flag(p.flags + u.tile * CM + rank, p.epoch);
             } else {
