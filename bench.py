@@ -64,6 +64,15 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
+def resolved_name(name: str, plan) -> str:
+    """The per-schedule name of what a plan runs: AUTO resolves to one of the
+    others, and its DRAM traffic is that schedule's."""
+    if name != "auto":
+        return name
+    kind = {0: "dp", 1: "persistent", 2: "streamk", 3: "splitk"}.get(plan.info("schedule"), "auto")
+    return "streamk_all" if kind == "streamk" and plan.info("sk_mode") == 1 else kind
+
+
 def profiled_traffic(workload: str, schedule: str):
     """DRAM bytes per launch from a committed ncu summary, if the kernel
     sources have not changed since it was taken (else None)."""
@@ -437,7 +446,7 @@ def main():
         achieved = alg_bytes / (launch_ms * 1e-3) / 1e9
         peak = pk["hbm_gbs"]
         unit = "GB/s"
-    traffic = profiled_traffic(spec["name"], sched)
+    traffic = profiled_traffic(spec["name"], resolved_name(sched, p))
     for s in per_sched:
         per_sched[s]["frac_of_%s_peak" % pk_src] = (
             per_sched[s]["tflops"] / pk["bf16_tflops"] if bound == "tensor"
