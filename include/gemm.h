@@ -146,13 +146,19 @@ enum {
      * Hilbert-curve scheduling).  The order is built on the host and copied
      * to a small device table owned by the plan when the option is set. */
     GEMM_OPT_RASTER = 13,
-    /* gemm_run_host: 0 (default) = pipelined in min(8, M / 512) row chunks
-     * when M >= 2048, else serial; 1 = always serial; 2..16 = that many row chunks (each a
-     * whole number of scheduled tile rows, so fewer may result).  Serial
-     * whenever the chunks' sub-plans would need more workspace than
-     * gemm_workspace_size of this plan.  GEMM_INFO_HOST_CHUNKS reports the
-     * count gemm_run_host uses. */
-    GEMM_OPT_HOST_CHUNKS = 14
+    /* gemm_run_host, row chunks of its block grid: 0 (default) = min(4,
+     * M / 1024) when M and N are both >= 2048, min(8, M / 512) when only M is,
+     * else 1; 1 = no row split; 2..16 = that many (each a whole number of
+     * scheduled tile rows, so fewer may result).  The whole call is serial when
+     * the grid has one block, or when the blocks' sub-plans would need more
+     * workspace than gemm_workspace_size of this plan.  GEMM_INFO_HOST_CHUNKS
+     * reports the count used. */
+    GEMM_OPT_HOST_CHUNKS = 14,
+    /* gemm_run_host, column chunks: 0 (default) = min(4, N / 1024) when M and
+     * N are both >= 2048, min(8, N / 512) when only N is, else 1; 1 = no
+     * column split; 2..16 = that many (whole tile columns).
+     * GEMM_INFO_HOST_COL_CHUNKS reports the count used. */
+    GEMM_OPT_HOST_COL_CHUNKS = 15
 };
 
 /* Keys for gemm_plan_get_info. */
@@ -178,7 +184,8 @@ enum {
     GEMM_INFO_SCHEDULE = 22,        /* the schedule that runs (GEMM_SCHED_AUTO resolved) */
     GEMM_INFO_SK_MODE = 23,         /* 1 when every tile is in the Stream-K wave */
     GEMM_INFO_RASTER = 24,          /* 0 grouped / linear, 1 Hilbert */
-    GEMM_INFO_HOST_CHUNKS = 25      /* row chunks gemm_run_host pipelines (1 = serial) */
+    GEMM_INFO_HOST_CHUNKS = 25,     /* row chunks of gemm_run_host's block grid */
+    GEMM_INFO_HOST_COL_CHUNKS = 26  /* column chunks (both 1: serial) */
 };
 
 /* Roles of a work unit reported by gemm_plan_units. */
@@ -240,12 +247,14 @@ gemm_status_t gemm_run(gemm_plan_t plan, const void *A, const void *B, void *C,
  * C = A * B on the device copies, and copies dC -> hC (device to host).  All
  * six buffers are the caller's, in the layouts of the plan; host buffers
  * should be pinned for the copies to be asynchronous.
- *  - Serial (GEMM_INFO_HOST_CHUNKS == 1): the three steps are enqueued on
- *    `stream`, the product through gemm_run.
- *  - Pipelined (GEMM_INFO_HOST_CHUNKS == n > 1, see GEMM_OPT_HOST_CHUNKS): B
- *    and then n row chunks of A are copied on an internal stream, chunk i of
- *    C is computed on `stream` once chunk i of A has arrived, and copied out
- *    on a second internal stream, so copies and compute overlap.  The call
+ *  - Serial (a one-block grid, see GEMM_OPT_HOST_CHUNKS and
+ *    GEMM_OPT_HOST_COL_CHUNKS): the three steps are enqueued on `stream`, the
+ *    product through gemm_run.
+ *  - Pipelined over an nr x nc grid of blocks: row chunks of A and column
+ *    chunks of B are copied in on an internal stream (A_0, B_0, A_1, B_1,
+ *    ...); block (i, j) of C is computed on `stream` once A_i and B_j have
+ *    arrived and copied out on a second internal stream, so copies and
+ *    compute overlap.  The call
  *    records an event on `stream` before its first copy and makes `stream`
  *    wait for the last copy out, so everything enqueued on `stream` before
  *    the call precedes it and everything after it follows it.  The first

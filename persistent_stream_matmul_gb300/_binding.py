@@ -37,13 +37,14 @@ GEMM_OPT_L2_PREFETCH = 11
 GEMM_OPT_PAIR_MMA = 12
 GEMM_OPT_RASTER = 13
 GEMM_OPT_HOST_CHUNKS = 14
+GEMM_OPT_HOST_COL_CHUNKS = 15
 
 INFO = {
     "tile_m": 1, "tile_n": 2, "tile_k": 3, "tiles_m": 4, "tiles_n": 5, "tiles": 6,
     "iters_per_tile": 7, "grid": 8, "sk_tiles": 9, "sk_iters_per_cta": 10,
     "sk_iters_rem": 11, "num_sms": 12, "stages": 13, "group_m": 14, "smem_bytes": 15, "cluster_m": 16,
     "a_rows_per_stage": 17, "split_k": 18, "k_rotate": 19,
-    "l2_prefetch": 20, "pair_mma": 21, "schedule": 22, "sk_mode": 23, "raster": 24, "host_chunks": 25,
+    "l2_prefetch": 20, "pair_mma": 21, "schedule": 22, "sk_mode": 23, "raster": 24, "host_chunks": 25, "host_col_chunks": 26,
 }
 ROLE_FULL, ROLE_OWNER, ROLE_PEER = 0, 1, 2
 
@@ -220,7 +221,7 @@ class Plan:
                 "sk_mode": GEMM_OPT_SK_MODE, "split_k": GEMM_OPT_SPLIT_K,
                 "k_rotate": GEMM_OPT_K_ROTATE, "l2_prefetch": GEMM_OPT_L2_PREFETCH,
                 "pair_mma": GEMM_OPT_PAIR_MMA, "raster": GEMM_OPT_RASTER,
-                "host_chunks": GEMM_OPT_HOST_CHUNKS}
+                "host_chunks": GEMM_OPT_HOST_CHUNKS, "host_col_chunks": GEMM_OPT_HOST_COL_CHUNKS}
         for k, v in options.items():
             if v is not None:
                 gemm_plan_set_option(self.handle, keys[k], int(v))

@@ -99,19 +99,22 @@ struct gemm_plan {
     int opt_grid, opt_group_m, opt_tile_n, opt_two_tiles, inject_skip, opt_cluster_m, opt_sk_mode;
     int opt_split, opt_k_rotate, opt_l2_prefetch, opt_pair_mma;
     int eff_schedule;  // the schedule that runs (GEMM_SCHED_AUTO resolved)
+    int eff_sk_mode;   // its Stream-K mode (GEMM_SCHED_AUTO resolved)
     int opt_raster;    // 0: grouped / linear (GROUP_M), 1: Hilbert curve
     std::vector<int32_t>* raster_host;  // Hilbert order, (row << 16) | column
     int32_t* raster_dev;                // device copy
     int64_t raster_tiles;               // entries in both
     int64_t wait_limit_us;
     int64_t a_ld;         // leading dimension of a column-major A in elements (0: M)
-    int opt_host_chunks;  // gemm_run_host: 0 auto, 1 serial, 2..16 row chunks
+    int64_t b_ld;         // leading dimension of a row-major B in elements (0: N)
+    int64_t c_ld;         // leading dimension of C in elements (0: N)
+    int opt_host_chunks;      // gemm_run_host row chunks: 0 auto, 1 none, 2..16
+    int opt_host_col_chunks;  // gemm_run_host column chunks: 0 auto, 1 none, 2..16
     // gemm_run_host pipeline, made on its first pipelined call
-    gemm_plan* sub_full;  // sub-plan over a full chunk of rows
-    gemm_plan* sub_last;  // sub-plan over the last (shorter) chunk, or null
-    int64_t sub_rows;     // rows of a full chunk
+    gemm_plan* sub[4];    // sub-plans: [last row chunk?][last column chunk?]
+    int64_t sub_rows, sub_cols;  // rows and columns of a full block
     cudaStream_t h2d, d2h;
-    cudaEvent_t ev_start, ev_done, ev_a[16], ev_c[16];
+    cudaEvent_t ev_start, ev_done, ev_a[16], ev_b[16], ev_c[64];
     bool pipe_ready;
     bool owns_status;     // false for a sub-plan: it reports into its parent's word
     int max_pair_ctas;  // CTAs co-resident as 2-CTA clusters (0: unknown)
@@ -270,6 +273,7 @@ gemm_status_t derive(gemm_plan* p) {
         }
     }
     p->eff_schedule = sched;
+    p->eff_sk_mode = sk_mode;
 
     Sched s{};
     s.tiles_m = (int32_t)tiles_m;
@@ -353,7 +357,11 @@ gemm_status_t derive(gemm_plan* p) {
     p->stages = stages_for(BN, p->AROWS, p->PAIR);
     p->smem_bytes = smem_for(BN, p->AROWS, p->PAIR);
     if (sched == GEMM_SCHED_STREAMK && s.sk_tiles > 0) {
-        p->ws_flag_bytes = ((size_t)s.sk_tiles * CM * 8 + 255) / 256 * 256;
+        // the hybrid rule splits fewer than 2g tiles whatever the shape: size
+        // the flags for 2g, so a plan over a block of this product (same grid)
+        // fits this workspace
+        const int64_t flag_tiles = sk_mode == 1 ? s.sk_tiles : std::max<int64_t>(s.sk_tiles, 2 * (int64_t)g);
+        p->ws_flag_bytes = ((size_t)flag_tiles * CM * 8 + 255) / 256 * 256;
         p->ws_bytes = p->ws_flag_bytes + (size_t)p->ctas * BM * BN * sizeof(float);
     } else if (sched == GEMM_SCHED_SPLITK && s.split > 1) {
         // one flag per tile half, one partial slot per (tile, part >= 1, half)
@@ -431,6 +439,7 @@ gemm_status_t make_plan(gemm_plan_t* out, int64_t M, int64_t N, int64_t K, int d
     p->wait_limit_us = 1000000;
     p->a_ld = 0;
     p->opt_host_chunks = 0;
+    p->opt_host_col_chunks = 0;
     p->owns_status = true;
     if (offline) {
         if (num_sms <= 0) { delete p; return GEMM_ERR_INVALID_ARG; }
@@ -518,7 +527,7 @@ gemm_status_t encode_maps(gemm_plan* p, const void* A, const void* B) {
             box[0] = BK; box[1] = (cuuint32_t)(p->BN / p->CM);  // each CTA of a pair loads half
         } else {
             dims[0] = (cuuint64_t)p->N; dims[1] = (cuuint64_t)p->K;
-            strides[0] = (cuuint64_t)p->N * 2;
+            strides[0] = (cuuint64_t)(p->b_ld ? p->b_ld : p->N) * 2;
             box[0] = 64; box[1] = BK;
         }
         if (enc(&p->tmB, dt, 2, const_cast<void*>(B), dims, strides, box, estr,
@@ -548,17 +557,17 @@ struct DeviceGuard {
 gemm_status_t run_impl(gemm_plan_t p, const void* A, const void* B, void* C, void* workspace,
                        gemm_stream_t stream, bool pdl);
 
-// Options of a sub-plan over some rows of the parent's product: the same
-// tile shape, cluster, schedule and options; A keeps the parent's leading
-// dimension.
+// Options of a sub-plan over a block of the parent's product: the same tile
+// shape, cluster, schedule and options; A, B and C keep the parent's leading
+// dimensions.
 void sub_options(const gemm_plan* p, gemm_plan* sp) {
     sp->opt_grid = p->opt_grid;
     sp->opt_group_m = p->opt_group_m;
     sp->opt_tile_n = p->BN;
     sp->opt_two_tiles = p->opt_two_tiles;
     sp->opt_cluster_m = p->CM;
-    sp->opt_sk_mode = p->opt_sk_mode;
-    // split-K: the parent's resolved part count, so every chunk sums in the
+    sp->opt_sk_mode = p->eff_sk_mode;
+    // split-K: the parent's resolved part count, so every block sums in the
     // parent's order (and a parent without partials gets sub-plans without)
     sp->opt_split = p->eff_schedule == GEMM_SCHED_SPLITK ? p->s.split : p->opt_split;
     sp->opt_k_rotate = p->opt_k_rotate;
@@ -566,16 +575,21 @@ void sub_options(const gemm_plan* p, gemm_plan* sp) {
     sp->opt_pair_mma = p->opt_pair_mma;
     sp->wait_limit_us = p->wait_limit_us;
     sp->a_ld = p->layout_a == GEMM_COL_MAJOR ? (p->a_ld ? p->a_ld : p->M) : 0;
+    sp->b_ld = p->layout_b == GEMM_ROW_MAJOR ? (p->b_ld ? p->b_ld : p->N) : 0;
+    sp->c_ld = p->c_ld ? p->c_ld : p->N;
 }
 
-// Workspace of a sub-plan over `rows` rows, from a scratch copy of the plan
-// (no raster table: it does not change the sizes and the copy builds none).
-bool sub_workspace(const gemm_plan* p, int64_t rows, size_t* flag_bytes, size_t* part_bytes) {
+// Workspace of a sub-plan over a rows x cols block, from a scratch copy of
+// the plan (no raster table: it does not change the sizes and the copy builds
+// none).
+bool sub_workspace(const gemm_plan* p, int64_t rows, int64_t cols, size_t* flag_bytes,
+                   size_t* part_bytes) {
     gemm_plan tmp = *p;
     tmp.raster_host = nullptr;
     tmp.raster_dev = nullptr;
     tmp.opt_raster = 0;
     tmp.M = rows;
+    tmp.N = cols;
     tmp.schedule = p->eff_schedule;
     sub_options(p, &tmp);
     if (derive(&tmp) != GEMM_OK) return false;
@@ -584,43 +598,85 @@ bool sub_workspace(const gemm_plan* p, int64_t rows, size_t* flag_bytes, size_t*
     return true;
 }
 
-// gemm_run_host: rows per chunk and chunk count.  Pipelining needs enough
-// rows for the copies of one chunk to hide the compute of another, and the
+// gemm_run_host: the block grid.  Row chunks are whole scheduled tile rows,
+// column chunks whole tile columns.  By default: with M >= 2048, row chunks
+// (at least 512 rows each, at most 8), which start after B has arrived; when
+// B is the larger operand (N > M), blocks of about a quarter of each side
+// instead, which start once one chunk of A and one of B have arrived; with
+// only N >= 2048, column chunks; serial otherwise.  The
 // sub-plans must fit the plan's workspace: their partials after one flag
-// region as large as either needs.
-int host_chunks(const gemm_plan* p, int64_t* rows_out) {
-    int n = 1;
-    if (p->opt_host_chunks != 1 && p->M > 0 && p->N > 0 && p->K > 0) {
+// region as large as any of them needs.
+int host_grid(const gemm_plan* p, int64_t* rows_out, int64_t* cols_out, int* nr_out, int* nc_out) {
+    int nr = 1, nc = 1;
+    if (p->M > 0 && p->N > 0 && p->K > 0) {
+        // a row chunk needs all of B and a column chunk all of A before its
+        // first block: split both sides only when B is the larger operand
+        const bool two_d = p->M >= 2048 && p->N > p->M;
         if (p->opt_host_chunks >= 2)
-            n = p->opt_host_chunks;
-        else if (p->M >= 2048)
-            n = (int)std::min<int64_t>(8, p->M / 512);  // chunks of at least 512 rows
+            nr = p->opt_host_chunks;
+        else if (p->opt_host_chunks == 0 && p->M >= 2048)
+            nr = (int)std::min<int64_t>(two_d ? 4 : 8, p->M / (two_d ? 1024 : 512));
+        if (p->opt_host_col_chunks >= 2)
+            nc = p->opt_host_col_chunks;
+        else if (p->opt_host_col_chunks == 0 && p->N >= 2048 && (two_d || p->M < 2048))
+            nc = (int)std::min<int64_t>(two_d ? 4 : 8, p->N / (two_d ? 1024 : 512));
     }
-    int64_t rows = p->M;
-    if (n > 1) {
-        const int64_t unit = (int64_t)BM * p->CM;  // whole scheduled tiles per chunk
-        rows = (p->M + n - 1) / n;
-        rows = (rows + unit - 1) / unit * unit;
-        n = (int)((p->M + rows - 1) / rows);
+    const int64_t unit_m = (int64_t)BM * p->CM, unit_n = p->BN > 0 ? p->BN : 128;
+    int64_t rows = p->M, cols = p->N;
+    if (nr > 1) {
+        rows = ((p->M + nr - 1) / nr + unit_m - 1) / unit_m * unit_m;
+        nr = (int)((p->M + rows - 1) / rows);
     }
-    if (n > 1) {
-        size_t f1 = 0, q1 = 0, f2 = 0, q2 = 0;
-        bool ok = sub_workspace(p, rows, &f1, &q1);
-        if (ok && p->M % rows) ok = sub_workspace(p, p->M % rows, &f2, &q2);
-        if (!ok || std::max(f1, f2) + std::max(q1, q2) > p->ws_bytes) n = 1;
+    if (nc > 1) {
+        cols = ((p->N + nc - 1) / nc + unit_n - 1) / unit_n * unit_n;
+        nc = (int)((p->N + cols - 1) / cols);
     }
-    if (n <= 1) {
-        n = 1;
+    if (nr < 1) nr = 1;
+    if (nc < 1) nc = 1;
+    if (nr == 1) rows = p->M;
+    if (nc == 1) cols = p->N;
+    while (nr * nc > 64) {  // events for at most 64 blocks
+        if (nc > 1) {
+            cols *= 2;
+            nc = (int)((p->N + cols - 1) / cols);
+        } else {
+            rows *= 2;
+            nr = (int)((p->M + rows - 1) / rows);
+        }
+    }
+    if (nr * nc > 1) {
+        size_t f = 0, q = 0;
+        const int64_t rs[2] = {rows, p->M % rows}, cs[2] = {cols, p->N % cols};
+        for (int i = 0; i < 2 && nr * nc > 1; ++i)
+            for (int j = 0; j < 2 && nr * nc > 1; ++j) {
+                if (rs[i] == 0 || cs[j] == 0) continue;
+                size_t fb = 0, pb = 0;
+                if (!sub_workspace(p, rs[i], cs[j], &fb, &pb)) {
+                    nr = nc = 1;
+                    break;
+                }
+                f = std::max(f, fb);
+                q = std::max(q, pb);
+            }
+        if (f + q > p->ws_bytes) nr = nc = 1;
+    }
+    if (nr * nc <= 1) {
+        nr = nc = 1;
         rows = p->M;
+        cols = p->N;
     }
     if (rows_out) *rows_out = rows;
-    return n;
+    if (cols_out) *cols_out = cols;
+    if (nr_out) *nr_out = nr;
+    if (nc_out) *nc_out = nc;
+    return nr * nc;
 }
 
-// A sub-plan over `rows` rows; device errors land in the parent's status word.
-gemm_status_t make_sub(gemm_plan* p, int64_t rows, gemm_plan** out) {
+// A sub-plan over a rows x cols block; device errors land in the parent's
+// status word.
+gemm_status_t make_sub(gemm_plan* p, int64_t rows, int64_t cols, gemm_plan** out) {
     gemm_plan* sp = nullptr;
-    gemm_status_t st = make_plan(&sp, rows, p->N, p->K, p->dtype, p->layout_a, p->layout_b,
+    gemm_status_t st = make_plan(&sp, rows, cols, p->K, p->dtype, p->layout_a, p->layout_b,
                                  p->eff_schedule, 0, 0);
     if (st != GEMM_OK) return st;
     sub_options(p, sp);
@@ -638,36 +694,44 @@ gemm_status_t make_sub(gemm_plan* p, int64_t rows, gemm_plan** out) {
 }
 
 void pipe_release(gemm_plan* p) {
-    if (p->sub_full) gemm_plan_destroy(p->sub_full);
-    if (p->sub_last) gemm_plan_destroy(p->sub_last);
-    p->sub_full = p->sub_last = nullptr;
+    for (gemm_plan*& sp : p->sub) {
+        if (sp) gemm_plan_destroy(sp);
+        sp = nullptr;
+    }
     // every handle is null until created, so a partly made pipeline is freed too
     if (p->h2d) cudaStreamDestroy(p->h2d);
     if (p->d2h) cudaStreamDestroy(p->d2h);
     if (p->ev_start) cudaEventDestroy(p->ev_start);
     if (p->ev_done) cudaEventDestroy(p->ev_done);
-    for (int i = 0; i < 16; ++i) {
-        if (p->ev_a[i]) cudaEventDestroy(p->ev_a[i]);
-        if (p->ev_c[i]) cudaEventDestroy(p->ev_c[i]);
-        p->ev_a[i] = p->ev_c[i] = nullptr;
+    for (cudaEvent_t& e : p->ev_a) {
+        if (e) cudaEventDestroy(e);
+        e = nullptr;
+    }
+    for (cudaEvent_t& e : p->ev_b) {
+        if (e) cudaEventDestroy(e);
+        e = nullptr;
+    }
+    for (cudaEvent_t& e : p->ev_c) {
+        if (e) cudaEventDestroy(e);
+        e = nullptr;
     }
     p->h2d = p->d2h = nullptr;
     p->ev_start = p->ev_done = nullptr;
     p->pipe_ready = false;
-    p->sub_rows = 0;
+    p->sub_rows = p->sub_cols = 0;
 }
 
-gemm_status_t pipe_prepare(gemm_plan* p, int64_t rows) {
-    if (p->pipe_ready && p->sub_rows == rows) return GEMM_OK;
+gemm_status_t pipe_prepare(gemm_plan* p, int64_t rows, int64_t cols) {
+    if (p->pipe_ready && p->sub_rows == rows && p->sub_cols == cols) return GEMM_OK;
     pipe_release(p);
     const unsigned ev_flags = cudaEventDisableTiming;
     bool ok = cudaStreamCreateWithFlags(&p->h2d, cudaStreamNonBlocking) == cudaSuccess;
     ok = ok && cudaStreamCreateWithFlags(&p->d2h, cudaStreamNonBlocking) == cudaSuccess;
     ok = ok && cudaEventCreateWithFlags(&p->ev_start, ev_flags) == cudaSuccess;
     ok = ok && cudaEventCreateWithFlags(&p->ev_done, ev_flags) == cudaSuccess;
-    for (int i = 0; i < 16 && ok; ++i)
-        ok = cudaEventCreateWithFlags(&p->ev_a[i], ev_flags) == cudaSuccess &&
-             cudaEventCreateWithFlags(&p->ev_c[i], ev_flags) == cudaSuccess;
+    for (cudaEvent_t& e : p->ev_a) ok = ok && cudaEventCreateWithFlags(&e, ev_flags) == cudaSuccess;
+    for (cudaEvent_t& e : p->ev_b) ok = ok && cudaEventCreateWithFlags(&e, ev_flags) == cudaSuccess;
+    for (cudaEvent_t& e : p->ev_c) ok = ok && cudaEventCreateWithFlags(&e, ev_flags) == cudaSuccess;
     if (!ok) {
         cudaGetLastError();
         pipe_release(p);
@@ -675,19 +739,23 @@ gemm_status_t pipe_prepare(gemm_plan* p, int64_t rows) {
     }
     p->pipe_ready = true;
     p->sub_rows = rows;
-    gemm_status_t st = make_sub(p, rows, &p->sub_full);
-    if (st == GEMM_OK && p->M % rows) st = make_sub(p, p->M % rows, &p->sub_last);
+    p->sub_cols = cols;
+    const int64_t rs[2] = {rows, p->M % rows}, cs[2] = {cols, p->N % cols};
+    gemm_status_t st = GEMM_OK;
+    for (int i = 0; i < 2 && st == GEMM_OK; ++i)
+        for (int j = 0; j < 2 && st == GEMM_OK; ++j)
+            if (rs[i] > 0 && cs[j] > 0 && !(rows == p->M && i == 1) && !(cols == p->N && j == 1))
+                st = make_sub(p, rs[i], cs[j], &p->sub[2 * i + j]);
     if (st != GEMM_OK) {
         pipe_release(p);
         return st;
     }
-    // both sub-plans share the caller's workspace: one flag region, as large
-    // as either needs, then the partials (host_chunks checked that it fits)
-    gemm_plan* subs[2] = {p->sub_full, p->sub_last};
+    // the sub-plans share the caller's workspace: one flag region, as large
+    // as any of them needs, then the partials (host_grid checked that it fits)
     size_t flags = 0;
-    for (gemm_plan* sp : subs)
+    for (gemm_plan* sp : p->sub)
         if (sp) flags = std::max(flags, sp->ws_flag_bytes);
-    for (gemm_plan* sp : subs)
+    for (gemm_plan* sp : p->sub)
         if (sp && sp->ws_bytes > 0) {
             sp->ws_bytes = flags + (sp->ws_bytes - sp->ws_flag_bytes);
             sp->ws_flag_bytes = flags;
@@ -775,6 +843,10 @@ gemm_status_t gemm_plan_set_option(gemm_plan_t p, int key, int64_t value) {
             if (value < 0 || value > 16) return GEMM_ERR_UNSUPPORTED;
             p->opt_host_chunks = (int)value;
             break;
+        case GEMM_OPT_HOST_COL_CHUNKS:
+            if (value < 0 || value > 16) return GEMM_ERR_UNSUPPORTED;
+            p->opt_host_col_chunks = (int)value;
+            break;
         default:
             return GEMM_ERR_INVALID_ARG;
     }
@@ -822,7 +894,18 @@ gemm_status_t gemm_plan_get_info(gemm_plan_t p, int key, int64_t* value) {
         case GEMM_INFO_PAIR_MMA: v = p->PAIR; break;
         case GEMM_INFO_SCHEDULE: v = p->eff_schedule; break;
         case GEMM_INFO_RASTER: v = p->opt_raster; break;
-        case GEMM_INFO_HOST_CHUNKS: v = host_chunks(p, nullptr); break;
+        case GEMM_INFO_HOST_CHUNKS: {
+            int nr = 1;
+            host_grid(p, nullptr, nullptr, &nr, nullptr);
+            v = nr;
+            break;
+        }
+        case GEMM_INFO_HOST_COL_CHUNKS: {
+            int nc = 1;
+            host_grid(p, nullptr, nullptr, nullptr, &nc);
+            v = nc;
+            break;
+        }
         case GEMM_INFO_SK_MODE: v = (p->eff_schedule == GEMM_SCHED_STREAMK && p->s.sk_tiles == p->s.tiles) ? 1 : 0; break;
         default: return GEMM_ERR_INVALID_ARG;
     }
@@ -856,8 +939,10 @@ gemm_status_t run_impl(gemm_plan_t p, const void* A, const void* B, void* C, voi
     if (!guard.ok) return GEMM_ERR_CUDA;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     if (p->K == 0) {  // empty sum: C = +0
-        return cudaMemsetAsync(C, 0, (size_t)p->M * p->N * 2, st) == cudaSuccess ? GEMM_OK
-                                                                                 : GEMM_ERR_CUDA;
+        const size_t ldc = (size_t)(p->c_ld ? p->c_ld : p->N);
+        return cudaMemset2DAsync(C, ldc * 2, 0, (size_t)p->N * 2, (size_t)p->M, st) == cudaSuccess
+                   ? GEMM_OK
+                   : GEMM_ERR_CUDA;
     }
     if (!A || !B) return GEMM_ERR_INVALID_ARG;
     if (((uintptr_t)A & 15u) || ((uintptr_t)B & 15u) || (p->K % 8) ||
@@ -887,6 +972,7 @@ gemm_status_t run_impl(gemm_plan_t p, const void* A, const void* B, void* C, voi
     kp.M = (int32_t)p->M;
     kp.N = (int32_t)p->N;
     kp.K = (int32_t)p->K;
+    kp.ldc = (int32_t)(p->c_ld ? p->c_ld : p->N);
     kp.C = C;
     kp.flags = p->ws_bytes ? reinterpret_cast<unsigned long long*>(workspace) : nullptr;
     kp.partials = p->ws_bytes
@@ -957,12 +1043,13 @@ gemm_status_t gemm_run_host(gemm_plan_t p, const void* hA, const void* hB, void*
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     const size_t a_bytes = (size_t)p->M * p->K * 2, b_bytes = (size_t)p->K * p->N * 2;
     const size_t c_bytes = (size_t)p->M * p->N * 2;
-    int64_t rows = 0;
-    int chunks = host_chunks(p, &rows);
+    int64_t rows = 0, cols = 0;
+    int nr = 1, nc = 1;
+    int blocks = host_grid(p, &rows, &cols, &nr, &nc);
     // the pipeline is a speed-up only: if its streams, events or sub-plans
     // cannot be made, run the serial path
-    if (chunks > 1 && pipe_prepare(p, rows) != GEMM_OK) chunks = 1;
-    if (chunks <= 1) {
+    if (blocks > 1 && pipe_prepare(p, rows, cols) != GEMM_OK) blocks = 1;
+    if (blocks <= 1) {
         if (p->K > 0) {
             if (cudaMemcpyAsync(dA, hA, a_bytes, cudaMemcpyHostToDevice, st) != cudaSuccess ||
                 cudaMemcpyAsync(dB, hB, b_bytes, cudaMemcpyHostToDevice, st) != cudaSuccess)
@@ -974,53 +1061,70 @@ gemm_status_t gemm_run_host(gemm_plan_t p, const void* hA, const void* hB, void*
             return GEMM_ERR_CUDA;
         return GEMM_OK;
     }
-    // Pipelined: B in, then row chunk i of A in (copy stream) -> chunk i of
-    // C computed (caller's stream) -> chunk i of C out (second copy stream),
-    // so the three overlap across chunks.  Entry and exit are ordered with
-    // the caller's stream through events.
-    const bool a_col = p->layout_a == GEMM_COL_MAJOR;
+    // Pipelined over an nr x nc grid of blocks: row chunks of A and column
+    // chunks of B are copied in on one internal stream, A_0, B_0, A_1, B_1, ...;
+    // block (i, j) is computed on `stream` once A_i and B_j have arrived, in
+    // the order their inputs complete, and copied out on a second internal
+    // stream.  Entry and exit are ordered with the caller's stream by events.
+    const bool a_col = p->layout_a == GEMM_COL_MAJOR, b_row = p->layout_b == GEMM_ROW_MAJOR;
     const char* ha = static_cast<const char*>(hA);
+    const char* hb = static_cast<const char*>(hB);
     char* da = static_cast<char*>(dA);
+    char* db = static_cast<char*>(dB);
     char* hc = static_cast<char*>(hC);
     char* dc = static_cast<char*>(dC);
+    const size_t M2 = (size_t)p->M * 2, N2 = (size_t)p->N * 2, K2 = (size_t)p->K * 2;
 #define PSM_CUDA(x) do { if ((x) != cudaSuccess) return GEMM_ERR_CUDA; } while (0)
     PSM_CUDA(cudaEventRecord(p->ev_start, st));
     PSM_CUDA(cudaStreamWaitEvent(p->h2d, p->ev_start, 0));
     PSM_CUDA(cudaStreamWaitEvent(p->d2h, p->ev_start, 0));
-    PSM_CUDA(cudaMemcpyAsync(dB, hB, b_bytes, cudaMemcpyHostToDevice, p->h2d));
-    for (int i = 0; i < chunks; ++i) {
-        const int64_t r0 = (int64_t)i * rows, nr = std::min(rows, p->M - r0);
-        if (!a_col) {
-            const size_t off = (size_t)r0 * p->K * 2;
-            PSM_CUDA(cudaMemcpyAsync(da + off, ha + off, (size_t)nr * p->K * 2, cudaMemcpyHostToDevice,
-                                     p->h2d));
-        } else {  // rows r0 .. r0+nr-1 of every column
-            PSM_CUDA(cudaMemcpy2DAsync(da + (size_t)r0 * 2, (size_t)p->M * 2, ha + (size_t)r0 * 2,
-                                       (size_t)p->M * 2, (size_t)nr * 2, (size_t)p->K,
-                                       cudaMemcpyHostToDevice, p->h2d));
+    for (int k = 0; k < std::max(nr, nc); ++k) {
+        if (k < nr) {  // rows r0 .. r0+n-1 of A
+            const int64_t r0 = (int64_t)k * rows, n = std::min(rows, p->M - r0);
+            if (!a_col)
+                PSM_CUDA(cudaMemcpyAsync(da + r0 * K2, ha + r0 * K2, n * K2, cudaMemcpyHostToDevice, p->h2d));
+            else
+                PSM_CUDA(cudaMemcpy2DAsync(da + r0 * 2, M2, ha + r0 * 2, M2, n * 2, (size_t)p->K,
+                                           cudaMemcpyHostToDevice, p->h2d));
+            PSM_CUDA(cudaEventRecord(p->ev_a[k], p->h2d));
         }
-        PSM_CUDA(cudaEventRecord(p->ev_a[i], p->h2d));
+        if (k < nc) {  // columns c0 .. c0+n-1 of B
+            const int64_t c0 = (int64_t)k * cols, n = std::min(cols, p->N - c0);
+            if (!b_row)
+                PSM_CUDA(cudaMemcpyAsync(db + c0 * K2, hb + c0 * K2, n * K2, cudaMemcpyHostToDevice, p->h2d));
+            else
+                PSM_CUDA(cudaMemcpy2DAsync(db + c0 * 2, N2, hb + c0 * 2, N2, n * 2, (size_t)p->K,
+                                           cudaMemcpyHostToDevice, p->h2d));
+            PSM_CUDA(cudaEventRecord(p->ev_b[k], p->h2d));
+        }
     }
     // The sub-plans and this plan share `workspace`, each with its own flag
     // layout: the sub-plans clear their (small) flag region on every call,
     // and this plan clears its own again on its next gemm_run.
-    p->sub_full->flags_cleared_for = nullptr;
-    if (p->sub_last) p->sub_last->flags_cleared_for = nullptr;
+    for (gemm_plan* sp : p->sub)
+        if (sp) sp->flags_cleared_for = nullptr;
     p->flags_cleared_for = nullptr;
-    for (int i = 0; i < chunks; ++i) {
-        const int64_t r0 = (int64_t)i * rows;
-        gemm_plan* sp = (i == chunks - 1 && p->sub_last) ? p->sub_last : p->sub_full;
-        const void* a_chunk = a_col ? (const void*)(da + (size_t)r0 * 2) : (const void*)(da + (size_t)r0 * p->K * 2);
-        PSM_CUDA(cudaStreamWaitEvent(st, p->ev_a[i], 0));
-        gemm_status_t r = run_impl(sp, a_chunk, dB, dc + (size_t)r0 * p->N * 2, workspace, stream, false);
-        if (r != GEMM_OK) return r;
-        PSM_CUDA(cudaEventRecord(p->ev_c[i], st));
-    }
-    for (int i = 0; i < chunks; ++i) {
-        const int64_t r0 = (int64_t)i * rows, nr = std::min(rows, p->M - r0);
-        PSM_CUDA(cudaStreamWaitEvent(p->d2h, p->ev_c[i], 0));
-        const size_t off = (size_t)r0 * p->N * 2;
-        PSM_CUDA(cudaMemcpyAsync(hc + off, dc + off, (size_t)nr * p->N * 2, cudaMemcpyDeviceToHost, p->d2h));
+    int done = 0;
+    for (int k = 0; k < std::max(nr, nc); ++k) {
+        // blocks whose later input is A_k or B_k: (k, 0..k) then (0..k-1, k)
+        for (int t = 0; t < 2 * k + 1; ++t) {
+            const int i = t <= k ? k : t - k - 1, j = t <= k ? t : k;
+            if (i >= nr || j >= nc) continue;
+            const int64_t r0 = (int64_t)i * rows, c0 = (int64_t)j * cols;
+            gemm_plan* sp = p->sub[2 * (i == nr - 1 && p->sub[2] ? 1 : 0) +
+                                   (j == nc - 1 && (p->sub[1] || p->sub[3]) ? 1 : 0)];
+            const void* a_blk = a_col ? (const void*)(da + r0 * 2) : (const void*)(da + r0 * K2);
+            const void* b_blk = b_row ? (const void*)(db + c0 * 2) : (const void*)(db + c0 * K2);
+            PSM_CUDA(cudaStreamWaitEvent(st, p->ev_a[i], 0));
+            PSM_CUDA(cudaStreamWaitEvent(st, p->ev_b[j], 0));
+            gemm_status_t r = run_impl(sp, a_blk, b_blk, dc + r0 * N2 + c0 * 2, workspace, stream, false);
+            if (r != GEMM_OK) return r;
+            PSM_CUDA(cudaEventRecord(p->ev_c[done], st));
+            PSM_CUDA(cudaStreamWaitEvent(p->d2h, p->ev_c[done], 0));
+            PSM_CUDA(cudaMemcpy2DAsync(hc + r0 * N2 + c0 * 2, N2, dc + r0 * N2 + c0 * 2, N2,
+                                       (size_t)sp->N * 2, (size_t)sp->M, cudaMemcpyDeviceToHost, p->d2h));
+            ++done;
+        }
     }
     PSM_CUDA(cudaEventRecord(p->ev_done, p->d2h));
     PSM_CUDA(cudaStreamWaitEvent(st, p->ev_done, 0));

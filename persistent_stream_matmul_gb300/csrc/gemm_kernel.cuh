@@ -94,6 +94,7 @@ struct Cfg {
 struct KParams {
     Sched s;
     int32_t M, N, K;
+    int32_t ldc;                 // elements between rows of C (N, or more for a block of a wider C)
     void* C;
     float* partials;             // Stream-K: grid slots of BM x BN fp32
     unsigned long long* flags;   // Stream-K: one flag per split tile
@@ -566,7 +567,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         cp_async_wait_all();
                     }
                 }
-                uint8_t* crow = reinterpret_cast<uint8_t*>(p.C) + ((size_t)row * p.N) * 2;
+                uint8_t* crow = reinterpret_cast<uint8_t*>(p.C) + ((size_t)row * p.ldc) * 2;
 #pragma unroll 1
                 for (int j = 0; j < BN / 32; ++j) {
                     uint32_t r[32];
@@ -671,7 +672,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         const uint4 v = ld_shared_u4(sbase + (uint32_t)(r * BN * 2) +
                                                      (uint32_t)((unit ^ (r & (C_UNITS - 1))) * 16));
                         if (col < p.N)
-                            st_u4(reinterpret_cast<uint8_t*>(p.C) + ((size_t)(tm * BM + r) * p.N + col) * 2,
+                            st_u4(reinterpret_cast<uint8_t*>(p.C) + ((size_t)(tm * BM + r) * p.ldc + col) * 2,
                                   v.x, v.y, v.z, v.w);
                     }
                 }

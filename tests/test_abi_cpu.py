@@ -98,7 +98,9 @@ def test_streamk_units_match_oracle(lib, M, N, K, sms, tile_n, cm):
         assert sorted(whole) == o.whole_tiles()
         ws = p.workspace_size
         if o.sk_tiles:
-            assert ws == -(-o.sk_tiles * cm * 8 // 256) * 256 + gu * cm * 128 * tile_n * 4
+            # flags for 2g split tiles (the most the hybrid rule makes), then a slot per CTA
+            flag_tiles = max(o.sk_tiles, 2 * gu)
+            assert ws == -(-flag_tiles * cm * 8 // 256) * 256 + gu * cm * 128 * tile_n * 4
         else:
             assert ws == 0
         p.close()
@@ -302,28 +304,37 @@ def test_hilbert_raster_matches_oracle(lib):
 
 
 def test_host_chunk_policy(lib):
-    """gemm_run_host pipelines whole-tile row chunks; the count follows
-    GEMM_OPT_HOST_CHUNKS, and it stays serial where the chunks' sub-plans
-    would not fit the plan's workspace."""
-    def chunks(M, sched, **opt):
-        p = B.Plan(M, 4096, 4096, B.GEMM_BF16, 0, 1, sched, offline_sms=152, **opt)
-        n = p.info("host_chunks")
-        rows = p.info("tile_m")
+    """gemm_run_host's block grid: row chunks of whole tile rows and column
+    chunks of whole tile columns; quarters of each side when both are long,
+    chunks of the long side only otherwise; serial when a side is short and
+    no split is asked for, or where the blocks' sub-plans would not fit the
+    plan's workspace."""
+    def grid(M, N, sched, **opt):
+        p = B.Plan(M, N, 4096, B.GEMM_BF16, 0, 1, sched, offline_sms=152, **opt)
+        out = (p.info("host_chunks"), p.info("host_col_chunks"), p.info("tile_m"), p.info("tile_n"))
         p.close()
-        return n, rows
-    assert chunks(8192, "persistent")[0] == 8
-    assert chunks(8192, "dp")[0] == 8
-    assert chunks(8192, "auto")[0] == 8          # AUTO resolves to hybrid Stream-K here
-    assert chunks(2048, "persistent")[0] == 4    # min(8, M / 512)
-    assert chunks(2047, "persistent")[0] == 1    # too few rows for the default
-    assert chunks(8192, "streamk")[0] == 8       # sub-plans fit the plan's workspace
-    assert chunks(8192, "splitk")[0] == 8
-    assert chunks(8192, "persistent", host_chunks=1)[0] == 1
-    # chunk rows round up to whole scheduled tiles: 1000 rows in 256-row tiles
-    # -> 3 requested chunks of 512 rows become 2
-    n, tm = chunks(1000, "persistent", host_chunks=3, cluster_m=2)
-    assert tm == 256 and n == 2
-    n, tm = chunks(1000, "persistent", host_chunks=16, cluster_m=1, tile_n=128)
-    assert tm == 128 and n == 8
+        return out
+    # B no larger than A: row chunks, min(8, M / 512)
+    assert grid(8192, 8192, "persistent")[:2] == (8, 1)
+    assert grid(8192, 8192, "auto")[:2] == (8, 1)
+    assert grid(8192, 8192, "streamk")[:2] == (8, 1)       # sub-plans fit the workspace
+    assert grid(8192, 8192, "splitk")[:2] == (8, 1)
+    assert grid(8192, 1024, "persistent")[:2] == (8, 1)
+    # B the larger operand: blocks, min(4, M / 1024) x min(4, N / 1024)
+    assert grid(2048, 4096, "persistent")[:2] == (2, 4)
+    assert grid(8192, 14336, "streamk")[:2] == (4, 4)
+    assert grid(8192, 14336, "auto")[:2] == (4, 4)
+    assert grid(64, 8192, "streamk")[:2] == (1, 8)         # only N is long: column chunks
+    assert grid(1024, 1024, "persistent")[:2] == (1, 1)    # serial
+    assert grid(8192, 8192, "persistent", host_chunks=1)[:2] == (1, 1)
+    assert grid(4096, 8192, "persistent", host_chunks=1)[:2] == (1, 4)
+    # chunks round up to whole tiles: 1000 rows in 256-row tiles -> 3 chunks of 512 rows become 2
+    n, nc, tm, tn = grid(1000, 1000, "persistent", host_chunks=3, host_col_chunks=3, cluster_m=2)
+    assert tm == 256 and n == 2 and nc == 3 and tn in (128, 256)
+    n, nc, tm, tn = grid(1000, 1024, "persistent", host_chunks=16, host_col_chunks=16, cluster_m=1,
+                         tile_n=128)
+    assert tm == 128 and tn == 128 and n == 8 and nc == 8
     with pytest.raises(B.GemmError):
-        chunks(1000, "persistent", host_chunks=17)
+        grid(1000, 1000, "persistent", host_chunks=17)
+    with pytest.raises(B.GemmError):
+        grid(1000, 1000, "persistent", host_col_chunks=17)

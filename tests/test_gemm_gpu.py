@@ -369,6 +369,49 @@ def test_run_host_pipelined_chunks(la, lb):
         p.close()
 
 
+@pytest.mark.parametrize("la,lb", LAYOUTS)
+def test_run_host_block_grid(la, lb):
+    # an nr x nc grid of blocks: column chunks of B (strided copies and a
+    # strided tensor map for a row-major B), blocks of C written with the full
+    # row stride and copied out as strided rectangles; ragged last blocks
+    M, N, K, dtype = 1000, 1040, 776, inputs.F16
+    A, Bm = inputs.operands(M, N, K, dtype, la, lb, inputs.INT_LAW, inputs.INT_LAW, 51)
+    _, _, Cref = oracle.gemm(A, Bm, M, N, K, dtype, la, lb)
+    hA = torch.from_numpy(A.view(np.int16).ravel()).pin_memory()
+    hB = torch.from_numpy(Bm.view(np.int16).ravel()).pin_memory()
+    dA, dB = hA.cuda(), hB.cuda()
+    dC = torch.empty(M * N, dtype=torch.int16, device="cuda")
+    stream = torch.cuda.current_stream()
+    for sched, opts in (("persistent", {}), ("streamk", {}), ("streamk", {"sk_mode": 1}),
+                        ("splitk", {}), ("dp", {"cluster_m": 1, "tile_n": 128})):
+        p = B.Plan(M, N, K, dtype, la, lb, sched, host_chunks=3, host_col_chunks=3, **opts)
+        assert p.info("host_chunks") * p.info("host_col_chunks") > 1, (sched, opts)
+        w = torch.zeros(max(1, p.workspace_size), dtype=torch.uint8, device="cuda")
+        for _ in range(2):
+            hC = torch.full((M * N,), 0x7E5A, dtype=torch.int16).pin_memory()
+            p.run_host(hA, hB, hC, dA, dB, dC, w if p.workspace_size else None, stream)
+            assert p.last_status(stream) == B.GEMM_OK
+            assert np.array_equal(hC.numpy().view(np.uint16).reshape(M, N), Cref), (sched, opts)
+        # the device copy of C is left in its row-major layout
+        assert np.array_equal(dC.cpu().numpy().view(np.uint16).reshape(M, N), Cref)
+        p.close()
+    # the automatic grid when B is the larger operand: 2 x 4 blocks
+    M, N = 2048, 4096
+    A, Bm = inputs.operands(M, N, 256, dtype, la, lb, inputs.INT_LAW, inputs.INT_LAW, 52)
+    _, _, Cref = oracle.gemm(A, Bm, M, N, 256, dtype, la, lb)
+    p = B.Plan(M, N, 256, dtype, la, lb, "auto")
+    assert (p.info("host_chunks"), p.info("host_col_chunks")) == (2, 4)
+    hA = torch.from_numpy(A.view(np.int16).ravel()).pin_memory()
+    hB = torch.from_numpy(Bm.view(np.int16).ravel()).pin_memory()
+    hC = torch.empty(M * N, dtype=torch.int16).pin_memory()
+    dC = torch.empty(M * N, dtype=torch.int16, device="cuda")
+    w = torch.zeros(max(1, p.workspace_size), dtype=torch.uint8, device="cuda")
+    p.run_host(hA, hB, hC, hA.cuda(), hB.cuda(), dC, w if p.workspace_size else None, stream)
+    assert p.last_status(stream) == B.GEMM_OK
+    assert np.array_equal(hC.numpy().view(np.uint16).reshape(M, N), Cref)
+    p.close()
+
+
 def test_run_host_splitk_chunks_keep_the_parents_part_count():
     # a split-K plan with one part per tile needs no workspace; its row-chunk
     # sub-plans keep that part count (found by a randomized parity sweep: they
