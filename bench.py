@@ -1,23 +1,32 @@
 #!/usr/bin/env python3
 """Benchmark: GEMM TFLOP/s (device-timed) and fraction of the GB300 roofline,
-per schedule, on one synthetic workload (default: bf16 8192 x 8192 x 8192,
-row-major A, column-major B).
+per schedule, on the five synthetic workloads.
 
-One step = one C = A*B through the C ABI (gemm_run) with the schedule that
-measured fastest in an untimed-for-the-headline per-schedule pass.  Prints
-one JSON line (rank 0).
+The headline workload (default: bf16 8192 x 8192 x 8192, row-major A,
+column-major B) gives the line's ``value``: K back-to-back steps of one
+C = A*B through the C ABI (gemm_run), with the schedule that measured fastest
+per launch.  The four other workloads get the same measurement under
+``per_workload`` (every schedule's per-launch median, the best schedule back
+to back, the roofline fraction: tensor, or HBM for the memory-bound skinny
+product).  Prints one JSON line.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
-                  [--schedule dp|persistent|streamk|best] [--impl ours|reference]
+  python bench.py [--steps K] [--warmup W] [--workload NAME]
+                  [--schedule dp|persistent|streamk|...|best] [--impl ours|reference]
+                  [--only-headline]
+
+The library issues cluster-multicast tensor copies from this GPU's own
+memory, so it runs on one GPU per process and is never part of a multi-GPU
+job: with --gpus > 1 or WORLD_SIZE > 1 this arm exits with an error before
+touching CUDA.
 
 --impl reference times the CPU oracle (the plain fp64 product) on the host
-cores instead, on a bounded row sample of the same workload per step.
-Under torchrun (N > 1) every rank runs its own copy of the workload (weak
-scaling, no collective on the data path); the timing is the max over ranks.
+cores instead, on a bounded row sample of the headline workload per step;
+under torchrun only rank 0 runs it.
 """
 from __future__ import annotations
 
 import argparse
+import datetime
 import hashlib
 import json
 import os
@@ -43,6 +52,8 @@ SCHED_NAMES = ["dp", "persistent", "streamk", "streamk_all", "splitk", "auto"]
 SCHED_DEFS = {"dp": ("dp", {}), "persistent": ("persistent", {}),
               "streamk": ("streamk", {}), "streamk_all": ("streamk", {"sk_mode": 1}),
               "splitk": ("splitk", {}), "auto": ("auto", {})}
+HEADLINE = "square8192_bf16"
+METRIC = "GEMM TFLOP/s (device-timed) and % of GB300 dense BF16 peak, per schedule"
 
 
 def peaks():
@@ -89,7 +100,9 @@ def profiled_traffic(workload: str, schedule: str):
 
 # --------------------------------------------------------------------- clocks
 class ClockSampler:
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi samples every 100 ms, with their timestamps, so that the
+    clocks of each measured phase can be told apart afterwards."""
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
     REASONS = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
@@ -97,6 +110,7 @@ class ClockSampler:
     def __init__(self, device_id: str | None):
         self.proc = None
         self.device_id = device_id
+        self.samples = []
         fd, self.path = tempfile.mkstemp(prefix="psm_clocks_", suffix=".csv")
         os.close(fd)
 
@@ -112,38 +126,59 @@ class ClockSampler:
         except Exception:
             self.proc = None
 
+    @staticmethod
+    def now() -> float:
+        """Local wall time in seconds, on the clock of nvidia-smi's timestamps."""
+        return datetime.datetime.now().timestamp()
+
+    @staticmethod
+    def parse(lines):
+        """[(t, sm_mhz, sm_max_mhz, power_w, {active reasons})] from the CSV."""
+        out = []
+        for line in lines:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                t = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                sm, smax, pw = float(parts[2]), float(parts[3]), float(parts[4])
+            except ValueError:
+                continue
+            reasons = {n for n, v in zip(ClockSampler.REASONS, parts[6:10])
+                       if v.lower().startswith("active")}
+            out.append((t, sm, smax, pw, reasons))
+        return out
+
     def stop(self):
         if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+            return
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
         except Exception:
             self.proc.kill()
         self.out.close()
-        sm, smax, power, reasons = [], [], [], set()
-        for line in open(self.path):
-            parts = [x.strip() for x in line.split(",")]
-            if len(parts) < 9:
-                continue
-            try:
-                sm.append(float(parts[1]))
-                smax.append(float(parts[2]))
-                power.append(float(parts[3]))
-            except ValueError:
-                continue
-            for name, val in zip(self.REASONS, parts[5:9]):
-                if val.lower().startswith("active"):
-                    reasons.add(name)
+        with open(self.path) as f:
+            self.samples = self.parse(f)
         try:
             os.unlink(self.path)
         except OSError:
             pass
-        busy = [s for s, p in zip(sm, power) if p > 0.5 * max(power)] if power else sm
-        return {"sm_mhz": statistics.median(busy) if busy else None,
-                "sm_max_mhz": max(smax) if smax else None,
-                "reasons": sorted(reasons), "samples": len(sm),
-                "power_w_max": max(power) if power else None}
+
+    def summary(self, t0: float | None = None, t1: float | None = None):
+        """Median SM clock under load, the maximum clock and the throttle
+        reasons seen, over all samples or those between t0 and t1."""
+        s = [x for x in self.samples if (t0 is None or x[0] >= t0) and (t1 is None or x[0] <= t1)]
+        if not s and t0 is not None and t1 is not None:
+            # a window shorter than the sampling period: the samples just around it
+            s = [x for x in self.samples if t0 - 0.15 <= x[0] <= t1 + 0.15]
+        if not s:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        pmax = max(x[3] for x in self.samples)
+        busy = [x[1] for x in s if x[3] > 0.5 * pmax] or [x[1] for x in s]
+        reasons = sorted(set().union(*(x[4] for x in s)))
+        return {"sm_mhz": statistics.median(busy), "sm_max_mhz": max(x[2] for x in s),
+                "reasons": reasons, "samples": len(s), "power_w_max": max(x[3] for x in s)}
 
 
 def device_pci_id(torch, dev: int):
@@ -203,19 +238,13 @@ def run_reference(args, spec, A, Bm):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": config_of(spec, "oracle", args.gpus),
+        "config": config_of(spec, "oracle"),
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle.num_threads(),
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
-
-
-METRIC = "GEMM TFLOP/s (device-timed) and % of GB300 dense BF16 peak, per schedule"
-
-
-L2_BYTES = 129e6
 
 
 def rotation_copies(spec) -> int:
@@ -225,13 +254,13 @@ def rotation_copies(spec) -> int:
     return max(1, min(512, int(np.ceil(2 * L2_BYTES / ab)))) if ab < 2 * L2_BYTES else 1
 
 
-def config_of(spec, schedule, n):
+def config_of(spec, schedule):
     return {"workload": spec["name"], "M": spec["M"], "N": spec["N"], "K": spec["K"],
             "dtype_in": "bf16" if spec["dtype"] == inputs.BF16 else "fp16",
             "accumulate": "fp32",
             "layout_a": "row" if spec["layout_a"] == 0 else "col",
             "layout_b": "row" if spec["layout_b"] == 0 else "col",
-            "schedule": schedule, "parallelism": "replica x%d" % n,
+            "schedule": schedule, "parallelism": "one GPU",
             "l2": l2_note(spec)}
 
 
@@ -244,20 +273,15 @@ def l2_note(spec) -> str:
         ab / 1e6, r, r * ab / 1e6)
 
 
-# --------------------------------------------------------------------- ranks
-def max_over_ranks(value: float, dist, world: int, device) -> float:
-    """Max of a per-rank number over all ranks (the slowest rank sets the time)."""
-    if world <= 1:
-        return float(value)
-    import torch
-    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
-    dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    return float(t.item())
-
-
-def whole_job_tflops(flops_per_step: float, steps: int, world: int, max_ms: float) -> float:
-    """Aggregate throughput: every rank ran `steps` steps; time = slowest rank."""
-    return world * steps * flops_per_step / (max_ms * 1e-3) / 1e12
+def multi_gpu_request(args, env) -> str | None:
+    """Why this arm refuses to run, or None: the library issues
+    cluster-multicast copies, so it stays on single-GPU runs."""
+    world = int(env.get("WORLD_SIZE", "1") or "1")
+    if args.gpus > 1 or world > 1:
+        return ("bench.py runs on one GPU only (--gpus %d, WORLD_SIZE %d): the library's "
+                "kernels use cluster-multicast tensor copies and are never run by a "
+                "multi-GPU job" % (args.gpus, world))
+    return None
 
 
 def sm_busy_fraction(stamps: np.ndarray, num_sms: int) -> dict:
@@ -271,50 +295,28 @@ def sm_busy_fraction(stamps: np.ndarray, num_sms: int) -> dict:
             "tail_us": float((last[-1] - np.median(last)) / 1e3)}
 
 
+def roofline_of(spec, ms: float, pk: dict):
+    """(bound, achieved, peak, unit) of one launch taking `ms` milliseconds:
+    tensor-bound products are rated in TFLOP/s against the bf16 dense peak
+    (fp16 has the same rate), memory-bound ones in GB/s of algorithmic bytes
+    2(MK + KN + MN) against the measured HBM copy bandwidth."""
+    M, N, K = spec["M"], spec["N"], spec["K"]
+    flops = 2.0 * M * N * K
+    alg_bytes = 2.0 * (M * K + K * N + M * N)
+    ridge = pk["bf16_tflops"] * 1e12 / (pk["hbm_gbs"] * 1e9)
+    if flops / alg_bytes >= ridge:
+        return "tensor", flops / (ms * 1e-3) / 1e12, pk["bf16_tflops"], "TFLOP/s"
+    return "hbm", alg_bytes / (ms * 1e-3) / 1e9, pk["hbm_gbs"], "GB/s"
+
+
 # --------------------------------------------------------------------- GPU arm
-def main():
-    ap = argparse.ArgumentParser()
-    ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=100)
-    ap.add_argument("--warmup", type=int, default=10)
-    ap.add_argument("--workload", default="square8192_bf16", choices=list(inputs.WORKLOADS))
-    ap.add_argument("--schedule", default="best", choices=SCHED_NAMES + ["best"])
-    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--reference-rows", type=int, default=16)
-    ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--no-e2e", action="store_true")
-    args = ap.parse_args()
-    if args.warmup < 3:
-        ap.error("--warmup must be >= 3")
-
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
-
-    if args.impl == "reference":
-        if rank != 0:
-            return
-        spec, A, Bm = inputs.workload(args.workload)
-        run_reference(args, spec, A, Bm)
-        return
-
-    import torch
-    import torch.distributed as dist
-
-    from persistent_stream_matmul_gb300 import _binding as B
-    from persistent_stream_matmul_gb300 import build
-
-    if world > 1:
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
-    torch.cuda.set_device(local_rank)
-    build.build()
-    B.load()
-
-    spec, A, Bm = inputs.workload(args.workload)
+def measure_workload(name, args, torch, B, sampler, pk, pk_src, headline):
+    """Per-schedule per-launch medians and the best (or chosen) schedule back
+    to back on one workload; for the headline also end to end."""
+    spec, A, Bm = inputs.workload(name)
     M, N, K, dtype = spec["M"], spec["N"], spec["K"], spec["dtype"]
     la, lb = spec["layout_a"], spec["layout_b"]
     flops = 2.0 * M * N * K
-    alg_bytes = 2.0 * (M * K + K * N + M * N)
     dA = torch.from_numpy(A.view(np.int16)).cuda()
     dB = torch.from_numpy(Bm.view(np.int16)).cuda()
     dC = torch.empty(M * N, dtype=torch.int16, device="cuda")
@@ -325,28 +327,23 @@ def main():
                              for _ in range(copies - 1)]
     stream = torch.cuda.current_stream()
 
+    chosen = args.schedule if headline else "best"
+    names = SCHED_NAMES if chosen == "best" else [chosen]
     plans, wss = {}, {}
-    for s in SCHED_NAMES:
+    for s in names:
         sched_kind, opts = SCHED_DEFS[s]
         plans[s] = B.Plan(M, N, K, dtype, la, lb, sched_kind, **opts)
         n = plans[s].workspace_size
         wss[s] = torch.zeros(n, dtype=torch.uint8, device="cuda") if n else None
 
-    def barrier():
-        if world > 1:
-            dist.barrier()
-
-    sampler = ClockSampler(device_pci_id(torch, local_rank))
-    sampler.start()
-
     # per-schedule device time (each launch bracketed by events on this stream),
     # in interleaved rounds so that every schedule samples the same drift of
     # the clocks under the power cap
     per_sched = {}
-    names = SCHED_NAMES if args.schedule == "best" else [args.schedule]
     rounds = 3
     per_round = max(1, -(-args.steps // rounds))
     times = {s: [] for s in names}
+    t_phase0 = sampler.now()
     for rnd in range(rounds):
         for s in names:
             p, w = plans[s], wss[s]
@@ -361,14 +358,18 @@ def main():
             torch.cuda.synchronize()
             st = p.last_status(stream)
             if st != B.GEMM_OK:
-                raise RuntimeError("device status after %s: %s" % (s, B.gemm_status_string(st)))
+                raise RuntimeError("device status after %s on %s: %s"
+                                   % (s, name, B.gemm_status_string(st)))
             times[s] += [ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(per_round)]
+    t_phase1 = sampler.now()
     for s in names:
         p, w = plans[s], wss[s]
         ms = times[s]
         med = statistics.median(ms)
+        bound, ach, peak, unit = roofline_of(spec, med, pk)
         per_sched[s] = {"tflops": flops / (med * 1e-3) / 1e12, "ms_median": med,
-                        "ms_min": min(ms), "ms_max": max(ms)}
+                        "ms_mean": statistics.fmean(ms), "ms_min": min(ms), "ms_max": max(ms),
+                        "frac_of_%s_peak" % pk_src: ach / peak}
         # one more (untimed) launch with per-CTA stamps: SM idle time at the tail
         ctas = p.info("grid")
         tbuf = torch.zeros(4 * ctas, dtype=torch.int64, device="cuda")
@@ -380,40 +381,60 @@ def main():
                                              p.info("num_sms")))
         per_sched[s]["ctas"] = ctas
         per_sched[s]["tile"] = "%dx%dx64" % (p.info("tile_m"), p.info("tile_n"))
+        per_sched[s]["runs"] = resolved_name(s, p)
 
     best = max(per_sched, key=lambda s: per_sched[s]["tflops"])
-    sched = best if args.schedule == "best" else args.schedule
+    sched = best if chosen == "best" else chosen
     p, w = plans[sched], wss[sched]
 
-    # headline: exactly K steps, barrier + synchronize on both sides, max over ranks
+    # back to back: exactly K steps, synchronize on both sides
     for i in range(args.warmup):
         p.run(*sets[i % copies], w, stream)
-    barrier()
     torch.cuda.synchronize()
+    t_head0 = sampler.now()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for i in range(args.steps):
         p.run(*sets[(args.warmup + i) % copies], w, stream)
     e1.record(stream)
     torch.cuda.synchronize()
-    barrier()
+    t_head1 = sampler.now()
     elapsed_ms = e0.elapsed_time(e1)
     if p.last_status(stream) != B.GEMM_OK:
-        raise RuntimeError("device status after the timed region is not OK")
-    elapsed_ms = max_over_ranks(elapsed_ms, dist, world, "cuda")
-    value = whole_job_tflops(flops, args.steps, world, elapsed_ms)
+        raise RuntimeError("device status after the timed region of %s is not OK" % name)
     launch_ms = elapsed_ms / args.steps
+    bound, achieved, peak, unit = roofline_of(spec, launch_ms, pk)
+
+    # after the timed region: the same burst with an event between launches,
+    # to show how launch times drift within a burst (clocks under the power cap)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    ev[0].record(stream)
+    for i in range(args.steps):
+        p.run(*sets[(args.warmup + i) % copies], w, stream)
+        ev[i + 1].record(stream)
+    torch.cuda.synchronize()
+    burst = [ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps)]
+    q = max(1, len(burst) // 4)
+    drift = {"ms_first_quarter": statistics.fmean(burst[:q]),
+             "ms_last_quarter": statistics.fmean(burst[-q:]),
+             "ms_median": statistics.median(burst)}
+
+    out = {"spec": spec, "A": A, "Bm": Bm, "schedule": sched, "plan": p,
+           "elapsed_ms": elapsed_ms, "launch_ms": launch_ms,
+           "tflops": flops / (launch_ms * 1e-3) / 1e12,
+           "per_schedule": per_sched, "burst_drift": drift,
+           "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
+                        "frac": achieved / peak},
+           "phases": {"per_schedule": (t_phase0, t_phase1), "back_to_back": (t_head0, t_head1)}}
 
     # end to end through the C ABI with host buffers: H2D A, B; GEMM; D2H C
-    e2e = None
-    if not args.no_e2e:
+    if headline and not args.no_e2e:
         hA = torch.from_numpy(A.view(np.int16)).reshape(-1).pin_memory()
         hB = torch.from_numpy(Bm.view(np.int16)).reshape(-1).pin_memory()
         hC = torch.empty(M * N, dtype=torch.int16).pin_memory()
         n_e2e = max(3, min(args.steps, 20))
         for _ in range(3):
             p.run_host(hA, hB, hC, dA, dB, dC, w, stream)
-        barrier()
         torch.cuda.synchronize()
         e2, e3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e2.record(stream)
@@ -421,59 +442,121 @@ def main():
             p.run_host(hA, hB, hC, dA, dB, dC, w, stream)
         e3.record(stream)
         torch.cuda.synchronize()
-        barrier()
-        te = max_over_ranks(e2.elapsed_time(e3), dist, world, "cuda")
-        e2e = {"value": whole_job_tflops(flops, n_e2e, world, te),
-               "unit": "TFLOP/s", "steps": n_e2e,
-               "h2d_bytes_per_step": int(hA.numel() * 2 + hB.numel() * 2),
-               "d2h_bytes_per_step": int(hC.numel() * 2),
-               "host_chunks": p.info("host_chunks")}
+        if p.last_status(stream) != B.GEMM_OK:
+            raise RuntimeError("device status after the end-to-end region is not OK")
+        te = e2.elapsed_time(e3)
+        out["e2e"] = {"value": n_e2e * flops / (te * 1e-3) / 1e12,
+                      "unit": "TFLOP/s", "steps": n_e2e,
+                      "h2d_bytes_per_step": int(hA.numel() * 2 + hB.numel() * 2),
+                      "d2h_bytes_per_step": int(hC.numel() * 2),
+                      "host_chunks": p.info("host_chunks"),
+                      "host_col_chunks": p.info("host_col_chunks")}
+    for s in names:
+        if s != sched:
+            plans[s].close()
+    return out
 
-    clocks = sampler.stop()
 
-    if rank != 0:
-        dist.destroy_process_group() if world > 1 else None
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default=HEADLINE, choices=list(inputs.WORKLOADS))
+    ap.add_argument("--schedule", default="best", choices=SCHED_NAMES + ["best"])
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--reference-rows", type=int, default=16)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--only-headline", action="store_true",
+                    help="measure the --workload alone, without per_workload")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    if args.impl == "reference":
+        if int(os.environ.get("RANK", "0")) != 0:
+            return
+        spec, A, Bm = inputs.workload(args.workload)
+        run_reference(args, spec, A, Bm)
         return
 
+    why = multi_gpu_request(args, os.environ)
+    if why:
+        print(why, file=sys.stderr, flush=True)
+        sys.exit(2)
+
+    import torch
+
+    from persistent_stream_matmul_gb300 import _binding as B
+    from persistent_stream_matmul_gb300 import build
+
+    torch.cuda.set_device(0)
+    build.build()
+    B.load()
     pk, pk_src = peaks()
-    ridge = pk["bf16_tflops"] * 1e12 / (pk["hbm_gbs"] * 1e9)
-    bound = "tensor" if flops / alg_bytes >= ridge else "hbm"
-    if bound == "tensor":
-        achieved = flops / (launch_ms * 1e-3) / 1e12
-        peak = pk["bf16_tflops"]       # fp16 and bf16 share the dense tensor rate
-        unit = "TFLOP/s"
-    else:
-        achieved = alg_bytes / (launch_ms * 1e-3) / 1e9
-        peak = pk["hbm_gbs"]
-        unit = "GB/s"
+
+    sampler = ClockSampler(device_pci_id(torch, 0))
+    sampler.start()
+    head = measure_workload(args.workload, args, torch, B, sampler, pk, pk_src, headline=True)
+    others = {}
+    if not args.only_headline:
+        for name in inputs.WORKLOADS:
+            if name == args.workload:
+                continue
+            r = measure_workload(name, args, torch, B, sampler, pk, pk_src, headline=False)
+            r.pop("plan").close()
+            r.pop("A"), r.pop("Bm")
+            others[name] = r
+            torch.cuda.empty_cache()
+    sampler.stop()
+
+    spec, p, sched = head["spec"], head["plan"], head["schedule"]
+    clocks = sampler.summary()
+    head_clk = sampler.summary(*head["phases"]["back_to_back"])
+    sched_clk = sampler.summary(*head["phases"]["per_schedule"])
     traffic = profiled_traffic(spec["name"], resolved_name(sched, p))
-    for s in per_sched:
-        per_sched[s]["frac_of_%s_peak" % pk_src] = (
-            per_sched[s]["tflops"] / pk["bf16_tflops"] if bound == "tensor"
-            else alg_bytes / (per_sched[s]["ms_median"] * 1e-3) / 1e9 / pk["hbm_gbs"])
+    rf = head["roofline"]
+
+    per_workload = {}
+    for name, r in [(args.workload, head)] + list(others.items()):
+        bt = sampler.summary(*r["phases"]["back_to_back"])
+        per_workload[name] = {
+            "config": config_of(r["spec"], r["schedule"]),
+            "best_schedule": r["schedule"],
+            "back_to_back_tflops": r["tflops"], "ms_per_step": r["launch_ms"],
+            "roofline": dict(r["roofline"], peak_source=pk_src + " (burst)",
+                             traffic=profiled_traffic(name, r["per_schedule"][r["schedule"]]["runs"])),
+            "sm_mhz_back_to_back": bt["sm_mhz"],
+            "burst_drift": r["burst_drift"],
+            "per_schedule": r["per_schedule"],
+        }
 
     line = {
-        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps,
+        "metric": METRIC, "value": head["tflops"], "unit": "TFLOP/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": head["launch_ms"],
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "bf16" if dtype == inputs.BF16 else "fp16", "data": "synthetic",
-        "config": config_of(spec, sched, world),
-        "per_schedule": per_sched,
-        "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
-                     "frac": achieved / peak, "peak_source": pk_src + " (burst)",
-                     "traffic": traffic, "algorithmic_bytes": alg_bytes,
+        "dtype": "bf16" if spec["dtype"] == inputs.BF16 else "fp16", "data": "synthetic",
+        "config": config_of(spec, sched),
+        "per_schedule": head["per_schedule"],
+        "roofline": {"bound": rf["bound"], "achieved": rf["achieved"], "peak": rf["peak"],
+                     "unit": rf["unit"], "frac": rf["frac"], "peak_source": pk_src + " (burst)",
+                     "traffic": traffic,
+                     "algorithmic_bytes": 2.0 * (spec["M"] * spec["K"] + spec["K"] * spec["N"]
+                                                 + spec["M"] * spec["N"]),
                      "kernel": "psm::gemm_kernel"},
         "gpu_launches": args.steps,
-        "clocks": clocks,
-        "e2e": e2e,
+        "clocks": dict(clocks, back_to_back=head_clk, per_schedule_rounds=sched_clk,
+                       headline_ms_x_sm_mhz=(head["launch_ms"] * head_clk["sm_mhz"]
+                                             if head_clk["sm_mhz"] else None)),
+        "e2e": head.get("e2e"),
+        "per_workload": per_workload,
     }
-    if not args.no_cpu_baseline and world == 1:
-        line["cpu_baseline"] = cpu_baseline(A, Bm, spec)
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(head["A"], head["Bm"], spec)
     else:
         line["cpu_baseline"] = None
     print(json.dumps(line), flush=True)
-    if world > 1:
-        dist.destroy_process_group()
 
 
 if __name__ == "__main__":

@@ -205,18 +205,28 @@ gemm_status_t gemm_plan_create(gemm_plan_t *out, int64_t M, int64_t N, int64_t K
 /*
  * Same as gemm_plan_create but touches no device: a plan for inspection only
  * (gemm_plan_get_info, gemm_plan_units, gemm_workspace_size) as if the device
- * had num_sms SMs.  gemm_run on it returns GEMM_ERR_NO_DEVICE.
+ * had num_sms SMs.  gemm_run on it returns GEMM_ERR_NO_DEVICE.  The pages
+ * have no counterpart (their wrapper derives the split at launch time).
+ * Errors: INVALID_ARG (as gemm_plan_create, or num_sms <= 0).
  */
 gemm_status_t gemm_plan_create_offline(gemm_plan_t *out, int64_t M, int64_t N, int64_t K,
                                        gemm_dtype_t dtype, gemm_layout_t layout_a,
                                        gemm_layout_t layout_b, gemm_schedule_t schedule,
                                        int num_sms);
 
-/* Set one GEMM_OPT_* option; the plan is re-derived.  Errors: INVALID_ARG
- * (NULL plan, unknown key), UNSUPPORTED (value out of range). */
+/* Set one GEMM_OPT_* option; the plan is re-derived.  The tuning options
+ * stand for the launch parameters of the issue's final version, matmul.apply
+ * (grid, block sizes, two_tiles) and the GROUP_M of swizzle_tile; the others
+ * (clusters, split-K parts, raster, host chunks, test hooks) have no
+ * counterpart on the pages.  On error the plan keeps its previous options.
+ * Errors: INVALID_ARG (NULL plan, unknown key), UNSUPPORTED (value out of
+ * range). */
 gemm_status_t gemm_plan_set_option(gemm_plan_t plan, int key, int64_t value);
 
-/* Read one GEMM_INFO_* value into *value.  Errors: INVALID_ARG. */
+/* Read one GEMM_INFO_* value into *value.  The derived counts (tiles,
+ * iterations per tile, Stream-K tiles, the even split) are those the issue's
+ * final version computes in its wrapper (_call); the rest have no counterpart
+ * on the pages.  Errors: INVALID_ARG (NULL plan or value, unknown key). */
 gemm_status_t gemm_plan_get_info(gemm_plan_t plan, int key, int64_t *value);
 
 /*
@@ -232,8 +242,11 @@ gemm_status_t gemm_plan_get_info(gemm_plan_t plan, int key, int64_t *value);
 gemm_status_t gemm_workspace_size(gemm_plan_t plan, size_t *bytes);
 
 /*
- * C = A * B on `stream`, asynchronously.  `workspace` may be NULL only when
- * gemm_workspace_size is 0.  C is written in full (every element, once);
+ * C = A * B on `stream`, asynchronously: one kernel launch.  Counterpart of
+ * the issue's final version, matmul.apply / _call, which launches the
+ * Stream-K kernel (first_wave) and then the whole-tile kernel (full_tiles);
+ * here one persistent launch runs both parts.  `workspace` may be NULL only
+ * when gemm_workspace_size is 0.  C is written in full (every element, once);
  * A and B are only read.  M == 0 or N == 0: nothing is done.  K == 0: C is
  * set to +0.
  * Errors: INVALID_ARG (NULL plan or operand), UNSUPPORTED (alignment),
@@ -243,7 +256,8 @@ gemm_status_t gemm_run(gemm_plan_t plan, const void *A, const void *B, void *C,
                        void *workspace, gemm_stream_t stream);
 
 /*
- * End-to-end variant: copies hA -> dA and hB -> dB (host to device), runs
+ * End-to-end variant (the pages time the device only and have no
+ * counterpart): copies hA -> dA and hB -> dB (host to device), runs
  * C = A * B on the device copies, and copies dC -> hC (device to host).  All
  * six buffers are the caller's, in the layouts of the plan; host buffers
  * should be pinned for the copies to be asynchronous.
@@ -297,7 +311,10 @@ gemm_status_t gemm_run_no_alloc(gemm_plan_t plan, const void *A, const void *B, 
 /*
  * Synchronise `stream`, then read and clear the plan's device status word.
  * Returns GEMM_OK, GEMM_ERR_TIMEOUT (a bounded device wait expired since the
- * last call), or GEMM_ERR_CUDA (the stream reported an error).
+ * last call), or GEMM_ERR_CUDA (the stream reported an error).  The pages
+ * have no counterpart: the spin lock of the issue's fixup waits without a
+ * bound and reports nothing.  Errors: INVALID_ARG (NULL plan), NO_DEVICE
+ * (offline plan).
  */
 gemm_status_t gemm_last_status(gemm_plan_t plan, gemm_stream_t stream);
 
@@ -316,7 +333,8 @@ gemm_status_t gemm_plan_units(gemm_plan_t plan, int64_t cta, int32_t *units,
                               int64_t max_units, int64_t *n_units);
 
 /*
- * Measurement hook: when `device_buffer` is not NULL, every later gemm_run of
+ * Measurement hook (no counterpart on the pages, which time whole launches
+ * only): when `device_buffer` is not NULL, every later gemm_run of
  * this plan writes four %globaltimer stamps (uint64 nanoseconds) per CTA into
  * it: CTA start, prologue done, last operand copy issued, CTA end; CTA c at
  * index 4*c.  It must hold at least 4 * 8 * GEMM_INFO_GRID bytes, else no
@@ -331,10 +349,15 @@ gemm_status_t gemm_plan_set_trace(gemm_plan_t plan, void *device_buffer, size_t 
 gemm_status_t gemm_plan_tile_coords(gemm_plan_t plan, int64_t tile, int64_t *tile_m,
                                     int64_t *tile_n);
 
-/* Free the plan and its device status word.  NULL is accepted. */
+/* Free the plan, its device status word, its raster table and the
+ * gemm_run_host pipeline (streams, events, sub-plans).  NULL is accepted.
+ * The pages have no counterpart (the Python wrapper frees nothing
+ * explicitly).  Always returns GEMM_OK. */
 gemm_status_t gemm_plan_destroy(gemm_plan_t plan);
 
-/* Static text for a status code (never NULL). */
+/* Static text for a status code (never NULL; unknown codes give
+ * "GEMM_ERR_UNKNOWN").  The pages have no counterpart: their error handling
+ * is assertions. */
 const char *gemm_status_string(gemm_status_t status);
 
 #ifdef __cplusplus

@@ -1099,8 +1099,12 @@ gemm_status_t gemm_run_host(gemm_plan_t p, const void* hA, const void* hB, void*
         }
     }
     // The sub-plans and this plan share `workspace`, each with its own flag
-    // layout: the sub-plans clear their (small) flag region on every call,
-    // and this plan clears its own again on its next gemm_run.
+    // layout.  Each sub-plan clears the shared flag region before its first
+    // block of this call; its later blocks (and blocks of the other
+    // sub-plan that follow them) find flags left by earlier runs and rely on
+    // the epoch tag: a post restarts a flag from another run at 1, and no
+    // wait matches another run's value.  This plan clears its own flags
+    // again on its next gemm_run.
     for (gemm_plan* sp : p->sub)
         if (sp) sp->flags_cleared_for = nullptr;
     p->flags_cleared_for = nullptr;

@@ -19,6 +19,8 @@ workloads the library is measured on; see ``WORKLOADS``.
 """
 from __future__ import annotations
 
+import os
+
 import numpy as np
 
 F16, BF16 = 0, 1
@@ -62,24 +64,11 @@ def uniform01(key: int, n: int, offset: int = 0) -> np.ndarray:
 
 
 def draw(law, key: int, n: int) -> np.ndarray:
-    """n doubles from a value law."""
-    kind = law[0]
-    if kind == "uniform":
-        lo, hi = law[1], law[2]
-        return lo + (hi - lo) * uniform01(key, n)
-    if kind == "normal":
-        sigma = law[1]
-        u = uniform01(key, 2 * n)
-        u1 = 1.0 - u[0::2]          # (0, 1]
-        u2 = u[1::2]
-        return sigma * (np.sqrt(-2.0 * np.log(u1)) * np.cos(2.0 * np.pi * u2))
-    if kind == "int":
-        lo, hi = law[1], law[2]
-        width = np.uint64(hi - lo + 1)
-        top = splitmix64(key, n) >> np.uint64(11)            # 53 bits
-        idx = (top * width) >> np.uint64(53)                  # 0 .. width-1
-        return idx.astype(np.float64) + lo
-    raise ValueError("unknown law %r" % (law,))
+    """n doubles from a value law: ``uniform`` (lo, hi) scales the uniform
+    doubles; ``normal`` (sigma) takes pairs of them through Box-Muller,
+    sqrt(-2 ln(1 - u1)) cos(2 pi u2); ``int`` (lo, hi) maps the top 53 bits
+    of each output to lo .. hi by a multiply-shift."""
+    return draw_range(law, key, 0, n)
 
 
 def to_bits(x: np.ndarray, dtype: int) -> np.ndarray:
@@ -102,15 +91,56 @@ def to_bits(x: np.ndarray, dtype: int) -> np.ndarray:
     raise ValueError("unknown dtype %r" % dtype)
 
 
-def matrix(rows: int, cols: int, layout: int, dtype: int, law, seed: int, matrix_id: int):
+def draw_range(law, key: int, start: int, n: int) -> np.ndarray:
+    """Values start .. start+n-1 of ``draw(law, key, total)`` for any total
+    above start+n: every law reads the counter-based stream at fixed
+    positions (value i of the normal law uses outputs 2i and 2i+1)."""
+    kind = law[0]
+    if kind == "uniform":
+        lo, hi = law[1], law[2]
+        return lo + (hi - lo) * uniform01(key, n, start)
+    if kind == "normal":
+        sigma = law[1]
+        u = uniform01(key, 2 * n, 2 * start)
+        u1 = 1.0 - u[0::2]
+        u2 = u[1::2]
+        return sigma * (np.sqrt(-2.0 * np.log(u1)) * np.cos(2.0 * np.pi * u2))
+    if kind == "int":
+        lo, hi = law[1], law[2]
+        width = np.uint64(hi - lo + 1)
+        top = splitmix64(key, n, start) >> np.uint64(11)
+        idx = (top * width) >> np.uint64(53)
+        return idx.astype(np.float64) + lo
+    raise ValueError("unknown law %r" % (law,))
+
+
+CHUNK = 1 << 22   # values per generator task
+
+
+def matrix(rows: int, cols: int, layout: int, dtype: int, law, seed: int, matrix_id: int,
+           chunk: int = CHUNK):
     """A rows x cols operand as uint16 patterns in its storage shape.
 
     Row-major storage has shape (rows, cols); column-major storage has shape
-    (cols, rows), i.e. element (r, c) is ``out[c, r]``.
+    (cols, rows), i.e. element (r, c) is ``out[c, r]``.  Large operands are
+    drawn in chunks on a thread pool (numpy releases the interpreter lock);
+    the stream is counter-based, so the bytes do not depend on the chunking.
     """
     key = (seed << 8) | matrix_id
-    vals = draw(law, key, rows * cols)
-    bits = to_bits(vals, dtype)
+    n = rows * cols
+    bits = np.empty(n, dtype=np.uint16)
+
+    def fill(start):
+        m = min(chunk, n - start)
+        bits[start:start + m] = to_bits(draw_range(law, key, start, m), dtype)
+
+    starts = range(0, n, chunk)
+    if len(starts) > 1:
+        from concurrent.futures import ThreadPoolExecutor
+        with ThreadPoolExecutor(max_workers=min(len(starts), os.cpu_count() or 1)) as ex:
+            list(ex.map(fill, starts))
+    elif n:
+        fill(0)
     shape = (rows, cols) if layout == ROW_MAJOR else (cols, rows)
     return bits.reshape(shape)
 

@@ -47,3 +47,27 @@ def test_storage_shapes_and_determinism():
     A, B = inputs.operands(5, 7, 3, inputs.BF16, inputs.COL_MAJOR, inputs.COL_MAJOR,
                            ("normal", 1.0), ("normal", 1.0), 1)
     assert A.shape == (3, 5) and B.shape == (7, 3)
+
+
+def test_chunked_draws_equal_one_draw():
+    # the generator pool cuts operands into chunks; the bytes must not change
+    for law in (("uniform", -1.0, 1.0), ("normal", 0.5), ("int", -2, 2)):
+        for dtype in (inputs.F16, inputs.BF16):
+            whole = inputs.to_bits(inputs.draw(law, 99, 1000), dtype).reshape(40, 25)
+            for chunk in (1, 7, 64, 999, 1000, 5000):
+                got = inputs.matrix(40, 25, inputs.ROW_MAJOR, dtype, law, 99 >> 8, 99 & 255,
+                                    chunk=chunk)
+                assert np.array_equal(got, whole), (law, dtype, chunk)
+
+
+def test_operand_bytes_are_stable():
+    # digests of the operands as the generator first produced them: the
+    # workloads' bytes must not change when the generator is reorganised
+    import hashlib
+    want = {(("uniform", -1.0, 1.0), 0): "6fd08b0bafdb0e3e", (("uniform", -1.0, 1.0), 1): "785c5cf6eca36cfb",
+            (("normal", 0.5), 0): "0dcdf3c465b4364f", (("normal", 0.5), 1): "fcc231cb818faf82",
+            (("int", -2, 2), 0): "8e0590bd0c8ac4ec", (("int", -2, 2), 1): "fb21f0fc867db2b1"}
+    for (law, dtype), digest in want.items():
+        for chunk in (inputs.CHUNK, 4096):
+            b = inputs.matrix(300, 70, inputs.ROW_MAJOR, dtype, law, 0x5EED0001, 1, chunk=chunk)
+            assert hashlib.sha256(b.tobytes()).hexdigest()[:16] == digest, (law, dtype, chunk)

@@ -140,3 +140,31 @@ def test_hilbert_curve_closed_forms():
         assert c[0] == (0, 0) and c[-1] == (n - 1, 0)
     t = hilbert_tiles(3, 5)
     assert sorted(t) == [(m, n) for m in range(3) for n in range(5)]
+
+
+def test_splitk_parts_hand_worked():
+    from oracle.streamk_schedule import splitk_parts
+    path = os.path.join(os.path.dirname(__file__), "golden", "splitk_parts.txt")
+    rows = 0
+    for line in open(path):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        head, parts = (x.strip() for x in line.split("|"))
+        ipt, S = (int(v) for v in head.split())
+        want = [tuple(int(v) for v in p.split(":")) for p in parts.split()]
+        assert splitk_parts(ipt, S) == want, (ipt, S)
+        rows += 1
+    assert rows == 7
+
+
+def test_splitk_parts_cover_the_tile_in_order():
+    # contiguous, ascending, non-empty when S <= ipt, sizes differ by at most one
+    from oracle.streamk_schedule import splitk_parts
+    for ipt in range(1, 70):
+        for S in range(1, ipt + 1):
+            parts = splitk_parts(ipt, S)
+            assert parts[0][0] == 0 and parts[-1][1] == ipt and len(parts) == S
+            assert all(a[1] == b[0] for a, b in zip(parts, parts[1:]))
+            sizes = [e - b for b, e in parts]
+            assert min(sizes) >= 1 and max(sizes) - min(sizes) <= 1
