@@ -46,12 +46,14 @@ from persistent_stream_matmul_gb300 import inputs  # noqa: E402
 
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_BYTES = 129e6
-SCHED_NAMES = ["dp", "persistent", "streamk", "streamk_all", "splitk", "auto"]
+SCHED_NAMES = ["dp", "persistent", "streamk", "streamk_all", "splitk", "splitk_cluster", "auto"]
 # name -> (schedule, options): "streamk" is the hybrid rule of the issue's final
-# version; "streamk_all" puts every tile in the Stream-K wave
+# version; "streamk_all" puts every tile in the Stream-K wave; "splitk_cluster"
+# reduces each tile's split-K parts inside a thread-block cluster
 SCHED_DEFS = {"dp": ("dp", {}), "persistent": ("persistent", {}),
               "streamk": ("streamk", {}), "streamk_all": ("streamk", {"sk_mode": 1}),
-              "splitk": ("splitk", {}), "auto": ("auto", {})}
+              "splitk": ("splitk", {}), "splitk_cluster": ("splitk", {"split_cluster": 1}),
+              "auto": ("auto", {})}
 HEADLINE = "square8192_bf16"
 METRIC = "GEMM TFLOP/s (device-timed) and % of GB300 dense BF16 peak, per schedule"
 
@@ -81,6 +83,8 @@ def resolved_name(name: str, plan) -> str:
     if name != "auto":
         return name
     kind = {0: "dp", 1: "persistent", 2: "streamk", 3: "splitk"}.get(plan.info("schedule"), "auto")
+    if kind == "splitk" and plan.info("split_k_cluster") == 1:
+        return "splitk_cluster"
     return "streamk_all" if kind == "streamk" and plan.info("sk_mode") == 1 else kind
 
 
@@ -295,6 +299,67 @@ def sm_busy_fraction(stamps: np.ndarray, num_sms: int) -> dict:
             "tail_us": float((last[-1] - np.median(last)) / 1e3)}
 
 
+def burst_sm_mhz(stamps: np.ndarray) -> list:
+    """Per launch: the median over CTAs of the SM clock each CTA ran at,
+    %clock64 cycles over %globaltimer nanoseconds (stamps: launches x CTAs x
+    (start, ready, loads done, end, clock at start, clock at end))."""
+    ns = stamps[:, :, 3].astype(np.float64) - stamps[:, :, 0]
+    cyc = stamps[:, :, 5].astype(np.float64) - stamps[:, :, 4]
+    with np.errstate(divide="ignore", invalid="ignore"):
+        ghz = np.where(ns > 0, cyc / ns, np.nan)
+    return [float(np.nanmedian(g)) * 1e3 for g in ghz]
+
+
+def host_link(torch, nbytes: int = 256 << 20):
+    """Pinned host <-> device copy bandwidth (GB/s, best of three) and the
+    NUMA placement of the GPU and of this process's CPUs: the end-to-end
+    number is bound by this link, which differs between boxes."""
+    out = {}
+    h = torch.empty(nbytes // 2, dtype=torch.int16).pin_memory()
+    d = torch.empty_like(h, device="cuda")
+    for name, fn in (("h2d_gbs", lambda: d.copy_(h, non_blocking=True)),
+                     ("d2h_gbs", lambda: h.copy_(d, non_blocking=True))):
+        best = 0.0
+        for _ in range(3):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            best = max(best, nbytes / (e0.elapsed_time(e1) * 1e-3) / 1e9)
+        out[name] = best
+    try:
+        bus = device_pci_id(torch, 0)
+        with open("/sys/bus/pci/devices/%s/numa_node" % bus.lower()[4:]) as f:
+            out["gpu_numa_node"] = int(f.read().strip())
+    except Exception:
+        out["gpu_numa_node"] = None
+    try:
+        cpus = os.sched_getaffinity(0)
+        nodes = set()
+        for n in os.listdir("/sys/devices/system/node"):
+            if n.startswith("node") and n[4:].isdigit():
+                with open("/sys/devices/system/node/%s/cpulist" % n) as f:
+                    if cpus & parse_cpulist(f.read()):
+                        nodes.add(int(n[4:]))
+        out["cpu_numa_nodes"] = sorted(nodes)
+        out["cpus"] = len(cpus)
+    except Exception:
+        out["cpu_numa_nodes"] = None
+    return out
+
+
+def parse_cpulist(text: str) -> set:
+    """'0-3,8,10-11' -> {0, 1, 2, 3, 8, 10, 11}"""
+    out = set()
+    for part in text.strip().split(","):
+        if not part:
+            continue
+        a, _, b = part.partition("-")
+        out.update(range(int(a), int(b or a) + 1))
+    return out
+
+
 def roofline_of(spec, ms: float, pk: dict):
     """(bound, achieved, peak, unit) of one launch taking `ms` milliseconds:
     tensor-bound products are rated in TFLOP/s against the bf16 dense peak
@@ -372,12 +437,12 @@ def measure_workload(name, args, torch, B, sampler, pk, pk_src, headline):
                         "frac_of_%s_peak" % pk_src: ach / peak}
         # one more (untimed) launch with per-CTA stamps: SM idle time at the tail
         ctas = p.info("grid")
-        tbuf = torch.zeros(4 * ctas, dtype=torch.int64, device="cuda")
+        tbuf = torch.zeros(B.TRACE_STAMPS * ctas, dtype=torch.int64, device="cuda")
         p.set_trace(tbuf, tbuf.numel() * 8)
         p.run(dA, dB, dC, w, stream)
         torch.cuda.synchronize()
         p.set_trace(None, 0)
-        per_sched[s].update(sm_busy_fraction(tbuf.cpu().numpy().reshape(ctas, 4),
+        per_sched[s].update(sm_busy_fraction(tbuf.cpu().numpy().reshape(ctas, B.TRACE_STAMPS),
                                              p.info("num_sms")))
         per_sched[s]["ctas"] = ctas
         per_sched[s]["tile"] = "%dx%dx64" % (p.info("tile_m"), p.info("tile_n"))
@@ -405,19 +470,31 @@ def measure_workload(name, args, torch, B, sampler, pk, pk_src, headline):
     launch_ms = elapsed_ms / args.steps
     bound, achieved, peak, unit = roofline_of(spec, launch_ms, pk)
 
-    # after the timed region: the same burst with an event between launches,
-    # to show how launch times drift within a burst (clocks under the power cap)
+    # after the timed region: the same burst again with an event between
+    # launches and per-CTA stamps in every launch, to show how launch times
+    # and the SM clock drift within a burst (the clock ramps after idle time
+    # and settles under the power cap)
+    ctas = p.info("grid")
+    n_st = B.TRACE_STAMPS
+    tb = torch.zeros(args.steps * n_st * ctas, dtype=torch.int64, device="cuda")
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    torch.cuda.synchronize()
     ev[0].record(stream)
     for i in range(args.steps):
+        p.set_trace(tb.data_ptr() + i * n_st * ctas * 8, n_st * ctas * 8)
         p.run(*sets[(args.warmup + i) % copies], w, stream)
         ev[i + 1].record(stream)
     torch.cuda.synchronize()
+    p.set_trace(None, 0)
     burst = [ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps)]
+    mhz = burst_sm_mhz(tb.cpu().numpy().reshape(args.steps, ctas, n_st))
     q = max(1, len(burst) // 4)
     drift = {"ms_first_quarter": statistics.fmean(burst[:q]),
              "ms_last_quarter": statistics.fmean(burst[-q:]),
-             "ms_median": statistics.median(burst)}
+             "ms_median": statistics.median(burst),
+             "sm_mhz_first_quarter": statistics.fmean(mhz[:q]),
+             "sm_mhz_last_quarter": statistics.fmean(mhz[-q:]),
+             "sm_mhz_median": statistics.median(mhz)}
 
     out = {"spec": spec, "A": A, "Bm": Bm, "schedule": sched, "plan": p,
            "elapsed_ms": elapsed_ms, "launch_ms": launch_ms,
@@ -450,7 +527,8 @@ def measure_workload(name, args, torch, B, sampler, pk, pk_src, headline):
                       "h2d_bytes_per_step": int(hA.numel() * 2 + hB.numel() * 2),
                       "d2h_bytes_per_step": int(hC.numel() * 2),
                       "host_chunks": p.info("host_chunks"),
-                      "host_col_chunks": p.info("host_col_chunks")}
+                      "host_col_chunks": p.info("host_col_chunks"),
+                      "host_link": host_link(torch)}
     for s in names:
         if s != sched:
             plans[s].close()

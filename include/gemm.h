@@ -25,8 +25,11 @@
  *                             (GEMM_OPT_SPLIT_K), computed by a persistent
  *                             grid and fixed up like Stream-K.
  *   GEMM_SCHED_AUTO           the plan picks one of the above from the shape
- *                             (GEMM_INFO_SCHEDULE and GEMM_INFO_SK_MODE report
- *                             which): Stream-K for a single row of tiles;
+ *                             (GEMM_INFO_SCHEDULE, GEMM_INFO_SK_MODE and
+ *                             GEMM_INFO_SPLIT_K_CLUSTER report which): split-K
+ *                             reduced inside clusters for a single row of
+ *                             128-row tiles when it fills one wave, else
+ *                             Stream-K for a single row of tiles;
  *                             persistent for tiny problems, for nearly one
  *                             full wave, and for 4+ waves of short tiles
  *                             (< 64 k-iterations, < 12 waves); Stream-K
@@ -106,12 +109,14 @@ enum {
     /* 1 (default): the issue's "two_tiles" rule adds g more Stream-K tiles
      * when more than g whole tiles would remain; 0: sk = tiles mod g. */
     GEMM_OPT_TWO_TILES = 4,
-    /* bound on a Stream-K owner's wait for its peers, microseconds (default
-     * 1000000).  On expiry the tile's C is not written and gemm_last_status
-     * reports GEMM_ERR_TIMEOUT. */
+    /* bound on a Stream-K or split-K owner's wait for its peers, and on a
+     * cluster split-K part's wait for the other parts of its tile,
+     * microseconds (default 1000000).  On expiry the waiting CTA does not
+     * write its part of C and gemm_last_status reports GEMM_ERR_TIMEOUT. */
     GEMM_OPT_WAIT_LIMIT_US = 5,
     /* test hook: the CTA with this index skips posting its peer flag, so its
-     * owner's wait runs out.  -1 (default) = off. */
+     * owner's wait runs out (cluster split-K: it skips signalling the other
+     * parts of its tile, whose waits run out).  -1 (default) = off. */
     GEMM_OPT_INJECT_SKIP_POST = 6,
     /* CTAs per cluster along M: 1, or 2 (two CTAs on adjacent 128-row halves
      * of a 256-row tile share one B tile, each loading half and multicasting
@@ -126,7 +131,8 @@ enum {
     GEMM_OPT_SK_MODE = 8,
     /* split-K parts per tile for GEMM_SCHED_SPLITK; 0 (default) = as many
      * as fit in one round of the grid, floor(units / tiles), at least 1 and
-     * at most ceil(K/64)/4. */
+     * at most ceil(K/64)/4.  With GEMM_OPT_SPLIT_K_CLUSTER: 2, 4 or 8, at
+     * most ceil(K/64). */
     GEMM_OPT_SPLIT_K = 9,
     /* k order of whole tiles: 1 = tile t starts at k-block t*ipt/tiles and
      * wraps around (changes only the fp32 summation order of those tiles),
@@ -158,7 +164,23 @@ enum {
      * N are both >= 2048, min(8, N / 512) when only N is, else 1; 1 = no
      * column split; 2..16 = that many (whole tile columns).
      * GEMM_INFO_HOST_COL_CHUNKS reports the count used. */
-    GEMM_OPT_HOST_COL_CHUNKS = 15
+    GEMM_OPT_HOST_COL_CHUNKS = 15,
+    /* GEMM_SCHED_SPLITK only.  0 (default): the parts of a tile meet through
+     * the workspace (fp32 partial slots and per-tile flags).  1: the S parts
+     * of a tile run as one thread-block cluster of S CTAs (S = 2, 4 or 8,
+     * GEMM_OPT_SPLIT_K; default the most that keep every tile in one wave),
+     * and add their fp32 partials through distributed shared memory in
+     * ascending k, so the plan needs no workspace; the sum order and so the
+     * result bits are those of the workspace form with the same S.  Tiles
+     * are 1-CTA (GEMM_OPT_CLUSTER_M = 2 and 64-wide tiles are UNSUPPORTED).
+     * Unless GEMM_OPT_TILE_N or GEMM_OPT_SPLIT_K fix them, the tile width
+     * (256 or 128) and S are the pair with the most CTAs in one wave of the
+     * grid (GEMM_OPT_GRID, default #SMs) whose clusters can all be resident
+     * at once, 256-wide tiles and then more parts first.  The grid is
+     * tiles x S CTAs.  A split of K reduced inside a cluster has
+     * no counterpart on the pages (the issue's closing comments name split-K
+     * only). */
+    GEMM_OPT_SPLIT_K_CLUSTER = 16
 };
 
 /* Keys for gemm_plan_get_info. */
@@ -177,7 +199,8 @@ enum {
     GEMM_INFO_SMEM_BYTES = 15,      /* dynamic shared memory per CTA */
     GEMM_INFO_CLUSTER_M = 16,       /* CTAs per cluster (1 or 2) */
     GEMM_INFO_A_ROWS_PER_STAGE = 17,/* rows of A each ring stage loads: 128, or 64 when M <= 64 */
-    GEMM_INFO_SPLIT_K = 18,         /* split-K parts per tile (0 unless GEMM_SCHED_SPLITK) */
+    GEMM_INFO_SPLIT_K = 18,         /* split-K parts per tile (0 unless GEMM_SCHED_SPLITK;
+                                       with GEMM_OPT_SPLIT_K_CLUSTER, the cluster size) */
     GEMM_INFO_K_ROTATE = 19,        /* 1 when whole tiles rotate their k order */
     GEMM_INFO_L2_PREFETCH = 20,     /* k-blocks of B prefetched into L2 ahead of the ring */
     GEMM_INFO_PAIR_MMA = 21,        /* 1 when the cluster runs pair MMAs */
@@ -185,11 +208,16 @@ enum {
     GEMM_INFO_SK_MODE = 23,         /* 1 when every tile is in the Stream-K wave */
     GEMM_INFO_RASTER = 24,          /* 0 grouped / linear, 1 Hilbert */
     GEMM_INFO_HOST_CHUNKS = 25,     /* row chunks of gemm_run_host's block grid */
-    GEMM_INFO_HOST_COL_CHUNKS = 26  /* column chunks (both 1: serial) */
+    GEMM_INFO_HOST_COL_CHUNKS = 26, /* column chunks (both 1: serial) */
+    GEMM_INFO_SPLIT_K_CLUSTER = 27, /* 1 when split-K parts reduce inside a cluster */
+    GEMM_INFO_CLUSTERS_RESIDENT = 28 /* clusters of this plan's kernel that fit the GPU at
+                                        once (0: no clusters, or an offline plan) */
 };
 
-/* Roles of a work unit reported by gemm_plan_units. */
-enum { GEMM_ROLE_FULL = 0, GEMM_ROLE_OWNER = 1, GEMM_ROLE_PEER = 2 };
+/* Roles of a work unit reported by gemm_plan_units.  CLUSTER_PART: one k-part
+ * of a tile under GEMM_OPT_SPLIT_K_CLUSTER, reduced with the other parts of
+ * its cluster. */
+enum { GEMM_ROLE_FULL = 0, GEMM_ROLE_OWNER = 1, GEMM_ROLE_PEER = 2, GEMM_ROLE_CLUSTER_PART = 3 };
 
 /*
  * Create a plan for one problem shape on the current CUDA device.
@@ -325,7 +353,8 @@ gemm_status_t gemm_last_status(gemm_plan_t plan, gemm_stream_t stream);
  * (raster order), first k-iteration,
  * end k-iteration, role (GEMM_ROLE_*), peers (for an OWNER: how many peer
  * partials it adds; else 0).  Writes at most max_units units to `units`
- * (may be NULL when max_units is 0) and the full count to *n_units.
+ * (may be NULL when max_units is 0) and the full count to *n_units.  For a
+ * CLUSTER_PART unit, peers holds the number of other parts of its tile.
  * Segments: issue, final version, first_wave (the range of a program cut at
  * tile boundaries) and full_tiles.  Errors: INVALID_ARG.
  */
@@ -335,10 +364,12 @@ gemm_status_t gemm_plan_units(gemm_plan_t plan, int64_t cta, int32_t *units,
 /*
  * Measurement hook (no counterpart on the pages, which time whole launches
  * only): when `device_buffer` is not NULL, every later gemm_run of
- * this plan writes four %globaltimer stamps (uint64 nanoseconds) per CTA into
- * it: CTA start, prologue done, last operand copy issued, CTA end; CTA c at
- * index 4*c.  It must hold at least 4 * 8 * GEMM_INFO_GRID bytes, else no
- * stamps are written.  The caller owns the buffer.  NULL turns stamps off.
+ * this plan writes six uint64 stamps per CTA into it: four %globaltimer
+ * stamps (nanoseconds) at CTA start, prologue done, last operand copy
+ * issued and CTA end, then the SM's %clock64 (cycles) at CTA start and end,
+ * whose ratio to the elapsed nanoseconds is the SM clock the CTA ran at; CTA
+ * c at index 6*c.  It must hold at least 6 * 8 * GEMM_INFO_GRID bytes, else
+ * no stamps are written.  The caller owns the buffer.  NULL turns stamps off.
  * Used to measure the idle time of SMs at the wave tail of each schedule.
  * Errors: INVALID_ARG (NULL plan or a buffer not 8-byte aligned).
  */

@@ -136,6 +136,15 @@ def splitk_parts(ipt: int, S: int):
     return [(p * ipt // S, (p + 1) * ipt // S) for p in range(S)]
 
 
+def cluster_split_units(tiles: int, ipt: int, S: int):
+    """Work of each CTA when the S split-K parts of every tile run as one
+    thread-block cluster (reading: CTA c takes part c mod S of tile c // S,
+    so the CTAs of a cluster -- consecutive indices -- are the parts of one
+    tile in ascending k).  Returns [(tile, k_begin, k_end)] indexed by CTA."""
+    parts = splitk_parts(ipt, S)
+    return [(c // S,) + parts[c % S] for c in range(tiles * S)]
+
+
 def hilbert_curve(order: int):
     """Cells (x, y) of the Hilbert curve on a 2^order square, in curve order,
     by the recursive construction: the curve of order n is four copies of the

@@ -38,6 +38,7 @@ GEMM_OPT_PAIR_MMA = 12
 GEMM_OPT_RASTER = 13
 GEMM_OPT_HOST_CHUNKS = 14
 GEMM_OPT_HOST_COL_CHUNKS = 15
+GEMM_OPT_SPLIT_K_CLUSTER = 16
 
 INFO = {
     "tile_m": 1, "tile_n": 2, "tile_k": 3, "tiles_m": 4, "tiles_n": 5, "tiles": 6,
@@ -45,8 +46,10 @@ INFO = {
     "sk_iters_rem": 11, "num_sms": 12, "stages": 13, "group_m": 14, "smem_bytes": 15, "cluster_m": 16,
     "a_rows_per_stage": 17, "split_k": 18, "k_rotate": 19,
     "l2_prefetch": 20, "pair_mma": 21, "schedule": 22, "sk_mode": 23, "raster": 24, "host_chunks": 25, "host_col_chunks": 26,
+    "split_k_cluster": 27, "clusters_resident": 28,
 }
-ROLE_FULL, ROLE_OWNER, ROLE_PEER = 0, 1, 2
+ROLE_FULL, ROLE_OWNER, ROLE_PEER, ROLE_CLUSTER_PART = 0, 1, 2, 3
+TRACE_STAMPS = 6   # uint64 per CTA written by gemm_plan_set_trace: 4 timer + 2 clock stamps
 
 # every entry point of include/gemm.h: name -> (restype, argtypes)
 _i64, _i32, _vp = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p
@@ -193,7 +196,8 @@ def gemm_plan_tile_coords(plan, tile: int):
 
 
 def gemm_plan_set_trace(plan, device_buffer, nbytes: int):
-    """Per-CTA %globaltimer stamps (start, ready, loads done, end) into a device buffer."""
+    """Per-CTA stamps into a device buffer: %globaltimer at start, ready,
+    loads done and end, then %clock64 at start and end (TRACE_STAMPS each)."""
     _check(load().gemm_plan_set_trace(plan, _addr(device_buffer), nbytes), "gemm_plan_set_trace")
 
 
@@ -221,7 +225,8 @@ class Plan:
                 "sk_mode": GEMM_OPT_SK_MODE, "split_k": GEMM_OPT_SPLIT_K,
                 "k_rotate": GEMM_OPT_K_ROTATE, "l2_prefetch": GEMM_OPT_L2_PREFETCH,
                 "pair_mma": GEMM_OPT_PAIR_MMA, "raster": GEMM_OPT_RASTER,
-                "host_chunks": GEMM_OPT_HOST_CHUNKS, "host_col_chunks": GEMM_OPT_HOST_COL_CHUNKS}
+                "host_chunks": GEMM_OPT_HOST_CHUNKS, "host_col_chunks": GEMM_OPT_HOST_COL_CHUNKS,
+                "split_cluster": GEMM_OPT_SPLIT_K_CLUSTER}
         for k, v in options.items():
             if v is not None:
                 gemm_plan_set_option(self.handle, keys[k], int(v))

@@ -32,6 +32,11 @@
 //               once, store C.  At a CTA's last unit the ring is idle: the
 //               peers' partials are copied into it in one round trip, and C
 //               is staged there and written as whole rows.
+//               CLUSTER_PART unit (cluster split-K): the fp32 partial goes
+//               to this CTA's idle ring; once every CTA of the cluster has
+//               signalled its own, each adds all parts of its slice of the
+//               tile's columns, read through distributed shared memory in
+//               ascending part order, rounds once and stores C.
 //
 // Sources: the HF post "naive vs persistent matmul" (tile per thread-block,
 // persistent thread-blocks, warp specialisation and double buffering named
@@ -88,7 +93,7 @@ struct Cfg {
     static_assert(AROWS == 128 || AROWS == 64, "rows of A per stage");
     static_assert(AROWS == 128 || A_STAGE_BYTES + B_STAGE_BYTES >= BM * BK * 2,
                   "the MMA's 128-row read of A must stay inside the stage");
-    static_assert((2 * STAGES + 5) * 8 + 8 <= BAR_BYTES, "barrier area");
+    static_assert((2 * STAGES + 6) * 8 + 8 <= BAR_BYTES, "barrier area");
 };
 
 struct KParams {
@@ -105,13 +110,18 @@ struct KParams {
     int32_t inject_skip_cta;     // test hook, -1 = off
     uint64_t wait_limit_ns;      // owner's wait for its peers
     uint64_t pipe_limit_ns;      // any wait inside the CTA's own pipeline
-    unsigned long long* trace;   // optional: 4 %globaltimer stamps per CTA, or null
+    unsigned long long* trace;   // optional: TRACE_N stamps per CTA, or null
 };
 
-// Per-CTA trace stamps (nanoseconds of %globaltimer): start of the CTA,
+// Per-CTA trace stamps: nanoseconds of %globaltimer at the start of the CTA,
 // prologue done (after the wait for earlier grids), last copy issued by the
-// producer, CTA end (all epilogue stores issued).
-enum : int { TRACE_START = 0, TRACE_READY = 1, TRACE_LOADS_DONE = 2, TRACE_END = 3, TRACE_N = 4 };
+// producer, CTA end (all epilogue stores issued); then the SM's %clock64 at
+// the start and at the end, so that (cycles / nanoseconds) is the SM clock
+// the CTA ran at.
+enum : int {
+    TRACE_START = 0, TRACE_READY = 1, TRACE_LOADS_DONE = 2, TRACE_END = 3,
+    TRACE_CLK_START = 4, TRACE_CLK_END = 5, TRACE_N = 6
+};
 
 __device__ __forceinline__ void record_status(int* status, int code) {
     atomicCAS(status, 0, code);
@@ -160,6 +170,62 @@ __device__ __forceinline__ bool epi_vote_all(bool v) {
 }
 
 template <bool OUT_BF16>
+__device__ __forceinline__ uint32_t pack2(float a, float b);
+
+// Cluster split-K: this CTA's slice of the tile, columns [part * BN / KC,
+// (part + 1) * BN / KC) of rows [0, rows), as 16-byte units of 4 fp32.  Every
+// CTA of the cluster holds its own part of the whole tile in its shared
+// memory at `sbase`, row r at r * BN * 4 bytes with unit u at
+// ((u ^ (r & 7)) * 16).  Each unit of the slice is the sum of the KC parts in
+// ascending part (= k) order, ((P0 + P1) + P2) + ..., in fp32, rounded once
+// and stored to C (tile origin `ctile`, row stride ldc elements, first column
+// col0).  The parts of BATCH units are loaded before any is added, so 16
+// loads are in flight per thread instead of one round trip per unit.
+template <int KC, int BN, bool OUT_BF16>
+__device__ __forceinline__ void cluster_reduce_slice(uint32_t sbase, int part, int rows, int et,
+                                                     uint8_t* ctile, int ldc, int col0, int N) {
+    constexpr int W4 = BN / 4 / KC;     // units of the slice in one row
+    constexpr int BATCH = 16 / KC;      // units per thread per round
+    constexpr uint32_t ROW_BYTES = (uint32_t)BN * 4;
+    const int total = rows * W4;
+#pragma unroll 1
+    for (int base = et; base < total; base += EPI_THREADS * BATCH) {
+        float4 x[BATCH][KC];
+#pragma unroll
+        for (int b = 0; b < BATCH; ++b) {
+            const int idx = base + b * EPI_THREADS;
+            if (idx < total) {
+                const int row = idx / W4;
+                const int gu = part * W4 + idx % W4;
+                const uint32_t a = sbase + (uint32_t)row * ROW_BYTES + (uint32_t)((gu ^ (row & 7)) * 16);
+#pragma unroll
+                for (int q = 0; q < KC; ++q)
+                    x[b][q] = q == part ? ld_shared_f4(a) : ld_cluster_f4(mapa_shared(a, (uint32_t)q));
+            }
+        }
+#pragma unroll
+        for (int b = 0; b < BATCH; ++b) {
+            const int idx = base + b * EPI_THREADS;
+            if (idx < total) {
+                const int row = idx / W4;
+                const int col = col0 + (part * W4 + idx % W4) * 4;
+                float4 acc = x[b][0];
+#pragma unroll
+                for (int q = 1; q < KC; ++q) {
+                    acc.x += x[b][q].x;
+                    acc.y += x[b][q].y;
+                    acc.z += x[b][q].z;
+                    acc.w += x[b][q].w;
+                }
+                if (col < N)
+                    st_u2(ctile + ((size_t)row * ldc + col) * 2, pack2<OUT_BF16>(acc.x, acc.y),
+                          pack2<OUT_BF16>(acc.z, acc.w));
+            }
+        }
+    }
+}
+
+template <bool OUT_BF16>
 __device__ __forceinline__ uint32_t pack2(float a, float b) {
     if constexpr (OUT_BF16) {
         __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
@@ -170,7 +236,9 @@ __device__ __forceinline__ uint32_t pack2(float a, float b) {
     }
 }
 
-template <int BN, bool OUT_BF16, int CM, int AROWS = 128, bool PAIR_MMA = false>
+// KCL: cluster split-K; the CTAs of a cluster (p.s.kc of them, along x) are
+// the k-parts of one tile and reduce through distributed shared memory.
+template <int BN, bool OUT_BF16, int CM, int AROWS = 128, bool PAIR_MMA = false, bool KCL = false>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ KParams p) {
@@ -180,6 +248,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     static_assert(BN >= 128 || CM == 1, "64-wide tiles only without clusters");
     constexpr int STAGES = Cf::STAGES;
     static_assert(CM == 1 || CM == 2, "cluster size");
+    static_assert(!KCL || (CM == 1 && !PAIR_MMA && BN >= 128), "cluster split-K: 1-CTA MMAs");
     constexpr uint16_t PAIR_MASK = 0x3;
     extern __shared__ uint8_t smem_raw[];
 
@@ -194,13 +263,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     auto tfull_bar = [&](int b) { return bar_base + 8u * (2 * STAGES + b); };
     auto tempty_bar = [&](int b) { return bar_base + 8u * (2 * STAGES + 2 + b); };
     const uint32_t done_bar = bar_base + 8u * (2 * STAGES + 4);
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_area + 8 * (2 * STAGES + 5));
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(bar_area + 8 * (2 * STAGES + 5) + 4);
+    const uint32_t parts_bar = bar_base + 8u * (2 * STAGES + 5);  // cluster split-K
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_area + 8 * (2 * STAGES + 6));
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(bar_area + 8 * (2 * STAGES + 6) + 4);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int cta = blockIdx.x;                      // workspace slot of this CTA
     const uint64_t t_start = globaltimer_ns();
+    const uint64_t c_start = sm_clock64();
     const int unit_cta = blockIdx.x / CM;            // index the scheduler knows
     const int rank = CM == 2 ? (int)cluster_ctarank() : 0;
 
@@ -217,6 +288,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             mbar_init(tempty_bar(b), (PAIR_MMA ? 2 : 1) * EPI_THREADS / 32);
         }
         mbar_init(done_bar, 1);
+        // one release-arrive from each other CTA of the cluster
+        if constexpr (KCL) mbar_init(parts_bar, (uint32_t)(p.s.kc > 1 ? p.s.kc - 1 : 1));
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -234,8 +307,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
     }
     tc_fence_before_sync();
-    if constexpr (CM == 2) {
-        cluster_sync_all();  // the peer's barriers exist before anything is multicast
+    if constexpr (CM == 2 || KCL) {
+        // the other CTAs' barriers exist before anything is multicast or
+        // arrives remotely
+        cluster_sync_all();
     } else {
         __syncthreads();
     }
@@ -470,6 +545,66 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const int row = tm * BM + row_in_tile;
             const bool row_ok = row_in_tile < rows_valid;
 
+            if constexpr (KCL) {
+                // every unit of a cluster split-K plan is a CLUSTER_PART
+                // The CTA's only unit: its ring is idle (every copy has landed
+                // and every MMA that read it has completed once this
+                // accumulator is ready), so the fp32 partial goes there, row
+                // by row with 16-byte units XOR-swizzled by row (conflict-free
+                // stores by the row-owning lanes).  An empty k-range
+                // contributes zeros.
+                constexpr uint32_t ROW_BYTES = (uint32_t)BN * 4;
+                static_assert((uint32_t)AROWS * ROW_BYTES <= (uint32_t)STAGES * Cf::STAGE_BYTES,
+                              "partial tile fits the ring");
+                const int kc = p.s.kc;
+                const int part = (int)cluster_ctarank();  // = u.slot: CTA c is part c mod kc
+                const bool empty = u.k1 <= u.k0;
+                fence_proxy_async_smem();
+                const uint32_t srow = sbase + (uint32_t)row_in_tile * ROW_BYTES;
+#pragma unroll 1
+                for (int j = 0; j < BN / 32; ++j) {
+                    uint32_t r[32];
+                    __syncwarp();
+                    tmem_ld_32x32b_x32(tbase + j * 32, r);
+                    if (row_ok) {
+#pragma unroll
+                        for (int v = 0; v < 8; ++v) {
+                            const int unit = (j * 8 + v) ^ (row_in_tile & 7);
+                            st_shared_u4(srow + (uint32_t)(unit * 16), empty ? 0u : r[4 * v],
+                                         empty ? 0u : r[4 * v + 1], empty ? 0u : r[4 * v + 2],
+                                         empty ? 0u : r[4 * v + 3]);
+                        }
+                    }
+                }
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(tempty_bar(buf));
+                // Every row of this part is in shared memory.  The barrier
+                // orders all epilogue threads' stores before thread 0's
+                // release-arrives on the other CTAs' barriers; their acquire
+                // waits then see the whole partial.
+                // (The test hook skips this CTA's signals, so the other parts'
+                // waits run out: they record a timeout and store nothing.)
+                named_bar_sync(BAR_EPI_SYNC, EPI_THREADS);
+                if (et == 0 && cta != p.inject_skip_cta) {
+#pragma unroll 1
+                    for (int q2 = 0; q2 < kc; ++q2)
+                        if (q2 != part) mbar_arrive_cluster(mapa_shared(parts_bar, (uint32_t)q2));
+                }
+                const bool got = mbar_wait_acq_cluster(parts_bar, 0, p.wait_limit_ns);
+                if (!epi_vote_all(got)) {
+                    if (et == 0) record_status(p.status, STATUS_FLAG_TIMEOUT);
+                } else {
+                    uint8_t* ctile = reinterpret_cast<uint8_t*>(p.C) + (size_t)tm * BM * p.ldc * 2;
+                    const int col0 = u.tn * BN;
+                    if (kc == 2)
+                        cluster_reduce_slice<2, BN, OUT_BF16>(sbase, part, rows_valid, et, ctile, p.ldc, col0, p.N);
+                    else if (kc == 4)
+                        cluster_reduce_slice<4, BN, OUT_BF16>(sbase, part, rows_valid, et, ctile, p.ldc, col0, p.N);
+                    else
+                        cluster_reduce_slice<8, BN, OUT_BF16>(sbase, part, rows_valid, et, ctile, p.ldc, col0, p.N);
+                }
+            } else {
             if (u.role == ROLE_PEER) {
                 // fp32 partial -> this CTA's slot, laid out [chunk][vec][row] so
                 // a warp's 16-byte stores cover 512 contiguous bytes
@@ -677,18 +812,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     }
                 }
             }
+            }  // not a cluster split-K part
             ++iter;
         }
     }
 
     tc_fence_before_sync();
     __syncwarp();
-    if constexpr (CM == 2) {
-        cluster_sync_all();  // neither CTA leaves while the other may still signal it
+    if constexpr (CM == 2 || KCL) {
+        // no CTA leaves while another may still signal it or read its
+        // shared memory
+        cluster_sync_all();
     } else {
         __syncthreads();
     }
-    if (p.trace && threadIdx.x == 0) p.trace[(size_t)cta * TRACE_N + TRACE_END] = globaltimer_ns();
+    if (p.trace && threadIdx.x == 0) {
+        p.trace[(size_t)cta * TRACE_N + TRACE_END] = globaltimer_ns();
+        p.trace[(size_t)cta * TRACE_N + TRACE_CLK_END] = sm_clock64();
+        p.trace[(size_t)cta * TRACE_N + TRACE_CLK_START] = c_start;
+    }
     if (warp == 1) {
         __syncwarp();
         tc_fence_after_sync();

@@ -21,6 +21,14 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
     return t;
 }
 
+// SM clock cycles (per-SM counter): with two %globaltimer stamps it gives the
+// SM clock a CTA ran at.
+__device__ __forceinline__ uint64_t sm_clock64() {
+    uint64_t c;
+    asm volatile("mov.u64 %0, %%clock64;" : "=l"(c) : : "memory");
+    return c;
+}
+
 __device__ __forceinline__ uint32_t elect_lane0() {
     return (threadIdx.x & 31) == 0;
 }
@@ -81,6 +89,34 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_
 #pragma unroll 1
         for (int i = 0; i < 32; ++i)
             if (mbar_try_wait(bar, parity)) return true;
+        if (globaltimer_ns() - t0 > limit_ns) return false;
+    }
+}
+
+// Same wait with acquire semantics at cluster scope: after it returns, this
+// thread sees the writes that other CTAs of the cluster made before their
+// release-arrive on this barrier (e.g. their shared memory, read through
+// distributed shared memory).
+__device__ __forceinline__ bool mbar_try_wait_acq_cluster(uint32_t bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+__device__ __forceinline__ bool mbar_wait_acq_cluster(uint32_t bar, uint32_t parity,
+                                                      uint64_t limit_ns) {
+    if (mbar_try_wait_acq_cluster(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+#pragma unroll 1
+        for (int i = 0; i < 32; ++i)
+            if (mbar_try_wait_acq_cluster(bar, parity)) return true;
         if (globaltimer_ns() - t0 > limit_ns) return false;
     }
 }
@@ -373,6 +409,21 @@ __device__ __forceinline__ uint4 ld_shared_u4(uint32_t addr) {
                  : "r"(addr)
                  : "memory");
     return v;
+}
+
+// 16 bytes of another CTA's shared memory (distributed shared memory);
+// `addr` is a shared::cluster address, e.g. from mapa.
+__device__ __forceinline__ float4 ld_cluster_f4(uint32_t addr) {
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(addr)
+                 : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_u2(void* p, uint32_t a, uint32_t b) {
+    asm volatile("st.global.v2.b32 [%0], {%1, %2};" ::"l"(p), "r"(a), "r"(b) : "memory");
 }
 
 __device__ __forceinline__ void st_f4(float4* p, float4 v) {

@@ -25,6 +25,11 @@
 // therefore finishes all its peer units before any owner unit, and owners
 // wait only on peers, which never wait.
 //
+// Cluster split-K (the same fixed split, reduced on chip): CTA c computes
+// part c mod kc of tile c / kc, once; the kc CTAs of a tile form one
+// thread-block cluster and add their fp32 partials through distributed
+// shared memory in ascending part order, so no workspace is involved.
+//
 // Fixup roles.  A unit that starts at k-iteration 0 of its tile and ends
 // before the tile's last iteration is the OWNER; a unit that starts past
 // iteration 0 is a PEER.  A CTA's range is contiguous, so only its first unit
@@ -43,7 +48,7 @@
 
 namespace psm {
 
-enum : int32_t { ROLE_FULL = 0, ROLE_OWNER = 1, ROLE_PEER = 2 };
+enum : int32_t { ROLE_FULL = 0, ROLE_OWNER = 1, ROLE_PEER = 2, ROLE_CLUSTER_PART = 3 };
 
 struct Sched {
     int32_t tiles_m, tiles_n, tiles;
@@ -56,6 +61,7 @@ struct Sched {
     int32_t k_rotate;    // 1: whole tiles start their k loop at their own
                          // offset (see unit_kblock)
     int32_t l2_prefetch; // k-blocks of B to prefetch into L2 ahead of the ring (0: off)
+    int32_t kc;          // cluster split-K: parts per tile = CTAs per cluster (0: off)
     const int32_t* raster_table;  // optional: tile id -> (row << 16) | column
     int64_t sk_q;        // Stream-K iterations per CTA (floor)
     int64_t sk_r;        // CTAs [0, sk_r) take sk_q + 1
@@ -65,10 +71,11 @@ struct Unit {
     int32_t tile;    // raster id
     int32_t k0, k1;  // k-iterations [k0, k1)
     int32_t role;
-    int32_t npeers;  // OWNER only
+    int32_t npeers;  // OWNER: peers it adds; CLUSTER_PART: the other parts of its tile
     int32_t tm, tn;  // tile row / column
     int32_t slot;    // PEER: its partial-tile slot; OWNER: slot of its first
-                     // peer (the peers' slots follow in ascending k)
+                     // peer (the peers' slots follow in ascending k);
+                     // CLUSTER_PART: its part (= its rank in the cluster)
 };
 
 struct Cursor {
@@ -155,6 +162,21 @@ PSM_HD bool cursor_next(const Sched& s, int32_t cta, Cursor& c, Unit& u) {
             u.npeers = (int32_t)(sk_cta_of(s, tile_first + s.ipt - 1) - cta);
             u.slot = cta + 1;
         }
+        tile_coords(s, u.tile, u.tm, u.tn);
+        return true;
+    }
+    if (s.kc > 0) {
+        const int64_t total = (int64_t)s.tiles * s.kc;
+        if (c.next_whole >= total) return false;
+        const int64_t uid = c.next_whole;
+        c.next_whole = 0x7FFFFFFF;  // one unit per CTA
+        const int32_t part = (int32_t)(uid % s.kc);
+        u.tile = (int32_t)(uid / s.kc);
+        u.k0 = (int32_t)(((int64_t)part * s.ipt) / s.kc);
+        u.k1 = (int32_t)(((int64_t)(part + 1) * s.ipt) / s.kc);
+        u.role = ROLE_CLUSTER_PART;
+        u.npeers = s.kc - 1;
+        u.slot = part;
         tile_coords(s, u.tile, u.tm, u.tn);
         return true;
     }

@@ -38,6 +38,7 @@ SCHEDULE_VARIANTS = {
     "streamk": ("streamk", {}),
     "streamk_all": ("streamk", {"sk_mode": 1}),
     "splitk": ("splitk", {}),
+    "splitk_cluster": ("splitk", {"split_cluster": 1}),
     "auto": ("auto", {}),
 }
 

@@ -163,7 +163,7 @@ def test_auto_schedule_choices(lib):
         (8192, 8192, 8192): (B.GEMM_SCHED_STREAMK, 0),
         (2304, 2304, 8192): (B.GEMM_SCHED_STREAMK, 1),
         (8192, 14336, 4096): (B.GEMM_SCHED_STREAMK, 0),
-        (64, 8192, 8192): (B.GEMM_SCHED_STREAMK, 1),
+        (64, 8192, 8192): (B.GEMM_SCHED_SPLITK, 0),
         # from the timed sweep of log-sampled shapes
         (3840, 2816, 5888): (B.GEMM_SCHED_STREAMK, 0),
         (768, 6656, 2304): (B.GEMM_SCHED_STREAMK, 1),
@@ -179,7 +179,29 @@ def test_auto_schedule_choices(lib):
     for (M, N, K), (sched, mode) in cases.items():
         p = B.Plan(M, N, K, B.GEMM_BF16, 0, 1, "auto", offline_sms=152)
         assert (p.info("schedule"), p.info("sk_mode")) == (sched, mode), (M, N, K)
+        assert p.info("split_k_cluster") == (1 if M <= 128 else 0), (M, N, K)
         p.close()
+
+
+def test_auto_single_row_of_tiles(lib):
+    # split-K reduced inside clusters when a choice of it fills one wave
+    for M, N, K, bn, S in ((64, 8192, 8192, 256, 4), (16, 1024, 4096, 128, 8),
+                           (128, 16384, 16384, 256, 2)):
+        p = B.Plan(M, N, K, B.GEMM_F16, 0, 0, "auto", offline_sms=152)
+        assert p.info("schedule") == B.GEMM_SCHED_SPLITK and p.info("split_k_cluster") == 1
+        assert (p.info("tile_n"), p.info("split_k"), p.workspace_size) == (bn, S, 0), (M, N, K)
+        p.close()
+    # otherwise Stream-K: one k-block (nothing to split), a forced pair
+    # cluster, or too many tiles for one wave of 2-part clusters
+    for M, N, K, opts in ((64, 8192, 64, {}), (64, 8192, 8192, {"cluster_m": 2}),
+                          (64, 65536, 4096, {})):
+        p = B.Plan(M, N, K, B.GEMM_F16, 0, 0, "auto", offline_sms=152, **opts)
+        assert p.info("split_k_cluster") == 0 and p.info("schedule") != B.GEMM_SCHED_SPLITK, (M, N, K)
+        p.close()
+    # the split-K part count of an AUTO plan does not leak into the choice
+    p = B.Plan(64, 8192, 8192, B.GEMM_F16, 0, 0, "auto", offline_sms=152, split_k=3)
+    assert (p.info("split_k_cluster"), p.info("split_k")) == (1, 4)
+    p.close()
 
 
 def test_half_height_a_for_short_m(lib):
@@ -338,3 +360,66 @@ def test_host_chunk_policy(lib):
         grid(1000, 1000, "persistent", host_chunks=17)
     with pytest.raises(B.GemmError):
         grid(1000, 1000, "persistent", host_col_chunks=17)
+
+@pytest.mark.parametrize("M,N,K", [(64, 8192, 8192), (300, 1000, 2048), (128, 256, 128), (1, 8, 4096)])
+def test_cluster_splitk_units_match_oracle(lib, M, N, K):
+    from oracle.streamk_schedule import cluster_split_units
+    for S in (0, 2, 4, 8):
+        try:
+            p = B.Plan(M, N, K, B.GEMM_F16, 0, 0, "splitk", offline_sms=152, split_cluster=1,
+                       split_k=S)
+        except B.GemmError as e:
+            assert e.status == B.GEMM_ERR_UNSUPPORTED and S > (K + 63) // 64
+            continue
+        tiles, ipt, S_got = p.info("tiles"), p.info("iters_per_tile"), p.info("split_k")
+        assert p.info("split_k_cluster") == 1 and p.info("cluster_m") == 1
+        assert p.info("tile_n") in (128, 256) and p.workspace_size == 0
+        if S:
+            assert S_got == S
+        assert S_got in (2, 4, 8) and S_got <= ipt
+        assert p.info("grid") == tiles * S_got
+        want = cluster_split_units(tiles, ipt, S_got)
+        for c in range(p.info("grid")):
+            units = p.units(c)
+            assert len(units) == 1
+            tile, k0, k1, role, npeers = units[0]
+            assert (tile, k0, k1) == want[c]
+            assert role == B.ROLE_CLUSTER_PART and npeers == S_got - 1
+        p.close()
+
+
+def test_cluster_splitk_defaults_and_refusals(lib):
+    # the skinny workload: 256-wide tiles, the most parts that keep one wave
+    p = B.Plan(64, 8192, 8192, B.GEMM_F16, 0, 0, "splitk", offline_sms=152, split_cluster=1)
+    assert (p.info("tile_n"), p.info("split_k"), p.info("grid")) == (256, 4, 128)
+    assert p.info("a_rows_per_stage") == 64 and p.info("schedule") == B.GEMM_SCHED_SPLITK
+    p.close()
+    # few tiles: 128-wide tiles when they put more CTAs in the wave (8 x 8
+    # against 4 x 8 at 256 wide)
+    p = B.Plan(128, 1024, 4096, B.GEMM_F16, 0, 0, "splitk", offline_sms=152, split_cluster=1)
+    assert (p.info("tile_n"), p.info("split_k"), p.info("grid")) == (128, 8, 64)
+    p.close()
+    # a tie (20 tiles x 4 parts or 40 x 2) goes to 256-wide tiles
+    p = B.Plan(64, 5120, 4096, B.GEMM_F16, 0, 0, "splitk", offline_sms=152, split_cluster=1)
+    assert (p.info("tile_n"), p.info("split_k"), p.info("grid")) == (256, 4, 80)
+    p.close()
+    # a wide product: no pair fits one wave, so 256-wide tiles and 2 parts
+    p = B.Plan(256, 20480, 4096, B.GEMM_BF16, 0, 1, "splitk", offline_sms=152, split_cluster=1)
+    assert (p.info("tile_n"), p.info("split_k"), p.info("grid")) == (256, 2, 320)
+    p.close()
+    p = B.Plan(64, 8192, 8192, B.GEMM_F16, 0, 0, "splitk", offline_sms=152)
+    for key, val in ((B.GEMM_OPT_SPLIT_K, 3), (B.GEMM_OPT_TILE_N, 64), (B.GEMM_OPT_CLUSTER_M, 2)):
+        q = B.Plan(64, 8192, 8192, B.GEMM_F16, 0, 0, "splitk", offline_sms=152)
+        q.set_option(key, val)
+        with pytest.raises(B.GemmError) as e:
+            q.set_option(B.GEMM_OPT_SPLIT_K_CLUSTER, 1)
+        assert e.value.status == B.GEMM_ERR_UNSUPPORTED
+        assert q.info("split_k_cluster") == 0          # the plan keeps its options
+        q.close()
+    with pytest.raises(B.GemmError):
+        p.set_option(B.GEMM_OPT_SPLIT_K_CLUSTER, 2)
+    p.close()
+    # other schedules ignore the option
+    p = B.Plan(64, 8192, 8192, B.GEMM_F16, 0, 0, "streamk", offline_sms=152, split_cluster=1)
+    assert p.info("split_k_cluster") == 0 and p.workspace_size > 0
+    p.close()

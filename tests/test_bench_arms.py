@@ -114,3 +114,14 @@ def test_reference_arm_line_on_rank_zero_only():
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
     assert d["config"]["workload"] == "square512_f16"
     assert _bench(args, {"RANK": "1", "WORLD_SIZE": "2"}) == []
+
+
+def test_burst_clock_and_cpulist_helpers():
+    # two launches x two CTAs: 1000 ns at 2000 and 1800 cycles per us
+    st = np.zeros((2, 2, 6), dtype=np.int64)
+    st[:, :, 3] = 1000
+    st[0, :, 5] = 2000
+    st[1, :, 5] = 1800
+    assert bench.burst_sm_mhz(st) == [2000.0, 1800.0]
+    assert bench.parse_cpulist("0-3,8,10-11\n") == {0, 1, 2, 3, 8, 10, 11}
+    assert bench.parse_cpulist("") == set()

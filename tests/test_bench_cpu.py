@@ -22,8 +22,8 @@ def test_rotation_keeps_the_operands_in_flight_above_twice_the_l2():
 
 
 class _FakePlan:
-    def __init__(self, schedule, sk_mode):
-        self._info = {"schedule": schedule, "sk_mode": sk_mode}
+    def __init__(self, schedule, sk_mode, split_cluster=0):
+        self._info = {"schedule": schedule, "sk_mode": sk_mode, "split_k_cluster": split_cluster}
 
     def info(self, key):
         return self._info[key]
@@ -35,6 +35,7 @@ def test_auto_files_its_traffic_under_the_schedule_it_resolves_to():
     assert bench.resolved_name("auto", _FakePlan(2, 0)) == "streamk"
     assert bench.resolved_name("auto", _FakePlan(2, 1)) == "streamk_all"
     assert bench.resolved_name("auto", _FakePlan(3, 0)) == "splitk"
+    assert bench.resolved_name("auto", _FakePlan(3, 0, 1)) == "splitk_cluster"
     assert bench.resolved_name("auto", _FakePlan(0, 0)) == "dp"
 
 

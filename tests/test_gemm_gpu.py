@@ -325,14 +325,16 @@ def test_trace_stamps_are_ordered(sched):
     A, Bm, dA, dB = _case(M, N, K, dtype, 0, 1, ("normal", 1.0), 14)
     p = B.Plan(M, N, K, dtype, 0, 1, sched)
     ctas = p.info("grid")
-    buf = torch.zeros(4 * ctas, dtype=torch.int64, device="cuda")
+    buf = torch.zeros(B.TRACE_STAMPS * ctas, dtype=torch.int64, device="cuda")
     p.set_trace(buf, buf.numel() * 8)
     Cb = run(p, dA, dB, M, N)
     _check_full(Cb, A, Bm, M, N, K, dtype, 0, 1)
-    t = buf.cpu().numpy().reshape(ctas, 4)
+    t = buf.cpu().numpy().reshape(ctas, B.TRACE_STAMPS)
     assert (t > 0).all()
     assert (t[:, 0] <= t[:, 1]).all() and (t[:, 1] <= t[:, 2]).all() and (t[:, 2] <= t[:, 3]).all()
     assert t[:, 3].max() - t[:, 0].min() < 10_000_000_000   # one run, well under 10 s
+    # the SM cycle counter moves forward over every CTA's lifetime
+    assert (t[:, 5] > t[:, 4]).all()
     p.set_trace(None, 0)
     p.close()
 

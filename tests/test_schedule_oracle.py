@@ -168,3 +168,16 @@ def test_splitk_parts_cover_the_tile_in_order():
             assert all(a[1] == b[0] for a, b in zip(parts, parts[1:]))
             sizes = [e - b for b, e in parts]
             assert min(sizes) >= 1 and max(sizes) - min(sizes) <= 1
+
+
+def test_cluster_split_units_hand_worked():
+    # two tiles of 10 k-iterations, four parts each (parts from the split-K
+    # golden reading: 10/4 = 2.5 -> 2, 20/4 = 5, 30/4 = 7.5 -> 7, 10)
+    from oracle.streamk_schedule import cluster_split_units
+    assert cluster_split_units(2, 10, 4) == [(0, 0, 2), (0, 2, 5), (0, 5, 7), (0, 7, 10),
+                                             (1, 0, 2), (1, 2, 5), (1, 5, 7), (1, 7, 10)]
+    # every (tile, k) exactly once, the CTAs of a cluster in ascending k
+    for tiles, ipt, S in ((3, 128, 4), (5, 9, 8), (1, 2, 2)):
+        units = cluster_split_units(tiles, ipt, S)
+        cover = sorted((t, k) for t, k0, k1 in units for k in range(k0, k1))
+        assert cover == [(t, k) for t in range(tiles) for k in range(ipt)]

@@ -19,7 +19,7 @@ pytestmark = pytest.mark.gpu
 # the schedules bench.py times, with its option sets
 SCHEDS = {"dp": ("dp", {}), "persistent": ("persistent", {}), "streamk": ("streamk", {}),
           "streamk_all": ("streamk", {"sk_mode": 1}), "splitk": ("splitk", {}),
-          "auto": ("auto", {})}
+          "splitk_cluster": ("splitk", {"split_cluster": 1}), "auto": ("auto", {})}
 
 
 @pytest.fixture(scope="module", autouse=True)

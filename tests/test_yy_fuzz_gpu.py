@@ -1,6 +1,6 @@
 """Randomized parity: random shapes, types, layouts, schedules and plan options
-(tile width, clusters, pair MMA, Stream-K mode and grid, split count, raster,
-host-buffer pipeline), integer-valued inputs, every result bit-exact against the
+(tile width, clusters, pair MMA, Stream-K mode and grid, split count, cluster
+split-K, raster, host-buffer pipeline), integer-valued inputs, every result bit-exact against the
 CPU oracle and identical on a second run.  A fixed seed keeps it reproducible.
 A sweep of this kind found a split-K host-pipeline case that the fixed tests had
 missed."""
@@ -43,6 +43,14 @@ def _random_case(rng: random.Random):
             opt["grid"] = rng.randint(1, 152)
     if sched == "splitk" and rng.random() < 0.5:
         opt["split_k"] = rng.randint(0, 9)
+    if sched == "splitk" and rng.random() < 0.4:
+        # parts reduced inside a cluster: 1-CTA tiles of 128 or 256 columns
+        opt["split_cluster"] = 1
+        opt["split_k"] = rng.choice([0, 2, 4, 8])
+        opt.pop("cluster_m", None)
+        opt.pop("pair_mma", None)
+        if opt.get("tile_n") == 64:
+            opt["tile_n"] = 128
     if rng.random() < 0.2:
         opt["raster"] = 1
     if rng.random() < 0.2 and sched != "dp":
