@@ -27,8 +27,9 @@
  *   GEMM_SCHED_AUTO           the plan picks one of the above from the shape
  *                             (GEMM_INFO_SCHEDULE, GEMM_INFO_SK_MODE and
  *                             GEMM_INFO_SPLIT_K_CLUSTER report which): split-K
- *                             reduced inside clusters for a single row of
- *                             128-row tiles when it fills one wave, else
+ *                             reduced inside clusters when it fits one wave
+ *                             (for more than one row of 128-row tiles, only
+ *                             with parts of at least 8 k-blocks); else
  *                             Stream-K for a single row of tiles;
  *                             persistent for tiny problems, for nearly one
  *                             full wave, and for 4+ waves of short tiles

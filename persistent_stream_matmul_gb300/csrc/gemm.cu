@@ -300,10 +300,13 @@ gemm_status_t kcl_shape(const gemm_plan* p, int64_t g, int* bn_out, int64_t* s_o
 gemm_status_t derive(gemm_plan* p) {
     const int64_t tiles_m128 = cdiv64(p->M, BM);
     // cluster split-K: the k-parts of a tile run as one cluster of 1-CTA MMAs.
-    // GEMM_SCHED_AUTO takes it for a single row of 128-row tiles (a skinny,
-    // memory-bound product) when some choice of it fills one wave: in a
-    // timed sweep of 45 such shapes (M 16-128, N 1024-16384, K 1024-16384) it
-    // was never slower than Stream-K and up to 2.8x faster.
+    // GEMM_SCHED_AUTO takes it when some choice of it fits one wave: for a
+    // single row of 128-row tiles (a skinny, memory-bound product) always --
+    // in a timed sweep of 45 such shapes (M 16-128, N 1024-16384, K
+    // 1024-16384) it was never slower than Stream-K and up to 2.8x faster --
+    // and for more rows when every part has at least 8 k-blocks: on the
+    // log-sampled shapes where it fits one wave it was 8-43 % faster than
+    // the other schedules with parts of 11-46 k-blocks, 25 % slower with 6.
     const int64_t g_kcl = p->opt_grid > 0 ? p->opt_grid : p->num_sms;
     bool kcl = p->schedule == GEMM_SCHED_SPLITK && p->opt_split_cluster == 1;
     int kcl_bn = 0;
@@ -311,12 +314,14 @@ gemm_status_t derive(gemm_plan* p) {
     if (kcl) {
         const gemm_status_t st = kcl_shape(p, g_kcl, &kcl_bn, &kcl_s);
         if (st != GEMM_OK) return st;
-    } else if (p->schedule == GEMM_SCHED_AUTO && tiles_m128 == 1 && p->K > BK &&
-               p->opt_cluster_m != 2 && p->opt_tile_n != 64) {
+    } else if (p->schedule == GEMM_SCHED_AUTO && p->K > BK && p->opt_cluster_m != 2 &&
+               p->opt_tile_n != 64) {
         bool fits = false;
         gemm_plan q = *p;
         q.opt_split = 0;  // the split-K part count does not apply to the other schedules
-        if (kcl_shape(&q, g_kcl, &kcl_bn, &kcl_s, &fits) == GEMM_OK && fits) kcl = true;
+        if (kcl_shape(&q, g_kcl, &kcl_bn, &kcl_s, &fits) == GEMM_OK && fits &&
+            (tiles_m128 == 1 || cdiv64(p->K, BK) >= 8 * kcl_s))
+            kcl = true;
     }
     // Tile width: 256 when that still gives every SM a tile (compute-bound
     // shapes: fewest operand bytes per FLOP); 64 for small problems with

@@ -11,7 +11,13 @@
   sample of the triples (seed 123); each shape timed with every schedule and
   with GEMM_SCHED_AUTO.  ``--large`` adds ``LARGE_SHAPES``, products of four or
   more waves of tiles that the sampler rarely draws under its size cap; the
-  rule for that regime in GEMM_SCHED_AUTO was fitted on them.
+  rule for that regime in GEMM_SCHED_AUTO was fitted on them.  ``--skinny``
+  times ``SKINNY_SHAPES`` (one row of 128-row tiles, fp16, row-major A and B,
+  the type and layouts of the skinny workload), on which AUTO's choice of
+  cluster split-K for single-row products was fitted.
+* ``--out`` keeps every record as JSON lines and ``--markdown`` renders them
+  as tables (per shape: each variant's TFLOP/s, what AUTO ran and its ratio to
+  the best variant; per variant: the geometric mean of its ratio to the best).
 
 * ``paired_compare``: two option sets (or schedules) on one shape, timed in
   short bursts that alternate between them (the order flips every pair), so
@@ -48,6 +54,11 @@ LARGE_SHAPES = [(8192, 8192, 8192), (8192, 14336, 4096), (4096, 4096, 4096), (16
                 (6144, 6144, 6144), (8192, 4096, 8192), (4096, 14336, 4096), (2048, 8192, 8192),
                 (3072, 3072, 8192), (12288, 12288, 2048), (4096, 8192, 2048), (8192, 8192, 1024),
                 (5120, 5120, 5120), (2560, 10240, 4096)]
+
+
+# one row of 128-row tiles: skinny, memory-bound products
+SKINNY_SHAPES = [(m, n, k) for m in (16, 64, 128) for n in (1024, 2048, 4096, 8192, 16384)
+                 for k in (1024, 4096, 16384)]
 
 
 def log_sampled_values(lo: int = 256, hi: int = 8192, step: int = 256, n: int = 1000):
@@ -110,8 +121,9 @@ def time_plan(ops: Operands, dtype, la, lb, schedule, options, warmup=3, iters=1
         us = statistics.median(ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(iters)) * 1e3
         flops = 2.0 * ops.M * ops.N * ops.K
         return {"us": us, "tflops": flops / (us * 1e-6) / 1e12,
-                "schedule": p.info("schedule"), "tile": "%dx%d" % (p.info("tile_m"), p.info("tile_n")),
-                "grid": p.info("grid")}
+                "schedule": p.info("schedule"), "sk_mode": p.info("sk_mode"),
+                "split_k_cluster": p.info("split_k_cluster"),
+                "tile": "%dx%d" % (p.info("tile_m"), p.info("tile_n")), "grid": p.info("grid")}
     except B.GemmError as e:
         return {"refused": str(e)}
     finally:
@@ -189,15 +201,67 @@ def shape_sweep(count, dtype=B.GEMM_BF16, la=0, lb=1, seed=123, max_macs=2.0 ** 
     t = torch_mod or t
     variants = variants or list(SCHEDULE_VARIANTS)
     rows = []
-    for (M, N, K) in list(sample_shapes(count, seed, max_macs)) + list(extra_shapes):
+    shapes = list(sample_shapes(count, seed, max_macs)) if count else []
+    for (M, N, K) in shapes + list(extra_shapes):
         ops = Operands(M, N, K, t)
         res = {}
         for name in variants:
             sched, opt = SCHEDULE_VARIANTS[name]
             res[name] = time_plan(ops, dtype, la, lb, sched, opt)
-        rows.append({"M": M, "N": N, "K": K, "results": res})
+        rows.append({"M": M, "N": N, "K": K, "dtype": "bf16" if dtype == B.GEMM_BF16 else "fp16",
+                     "layout_a": la, "layout_b": lb, "results": res})
         del ops
     return rows
+
+
+def auto_runs(r: dict) -> str:
+    """The variant name of what AUTO resolved to, from its timing record."""
+    kind = {0: "dp", 1: "persistent", 2: "streamk", 3: "splitk"}.get(r.get("schedule"), "?")
+    if kind == "splitk" and r.get("split_k_cluster"):
+        return "splitk_cluster"
+    if kind == "streamk" and r.get("sk_mode"):
+        return "streamk_all"
+    return kind
+
+
+def markdown(rows, title: str) -> str:
+    """A shape sweep as a table: TFLOP/s per variant, AUTO's choice and its
+    ratio to the best variant, then the geometric means of summarize_shapes."""
+    if not rows:
+        return ""
+    names = [n for n in rows[0]["results"] if n != "auto"]
+    out = ["## " + title, "",
+           "| M | N | K | " + " | ".join(names) + " | auto (runs) | auto / best |",
+           "|---:|---:|---:|" + "---:|" * len(names) + "---|---:|"]
+    for r in rows:
+        res = r["results"]
+        best = max(v.get("tflops", 0.0) for v in res.values())
+        cells = []
+        for n in names:
+            v = res[n].get("tflops")
+            cells.append(("**%.1f**" if v == best else "%.1f") % v if v else "-")
+        a = res.get("auto", {})
+        cells.append("%.1f (%s)" % (a["tflops"], auto_runs(a)) if a.get("tflops") else "-")
+        cells.append("%.3f" % (a["tflops"] / best) if a.get("tflops") and best else "-")
+        out.append("| %d | %d | %d | " % (r["M"], r["N"], r["K"]) + " | ".join(cells) + " |")
+    out += ["", "Geometric mean of each variant's TFLOP/s over the best variant of the shape:", ""]
+    for n, v in summarize_shapes(rows).items():
+        out.append("- %s: %.4f (best on %d of %d shapes)" % (n, v["geomean_vs_best"], v["wins"], v["shapes"]))
+    return "\n".join(out) + "\n"
+
+
+def grid_markdown(rows) -> str:
+    if not rows:
+        return ""
+    r0 = rows[0]
+    out = ["## Stream-K grid sweep, %d x %d x %d" % (r0["M"], r0["N"], r0["K"]), "",
+           "| grid (CTAs) | two_tiles | us | TFLOP/s |", "|---:|---:|---:|---:|"]
+    for r in sorted(rows, key=lambda r: (-r["two_tiles"], r["grid"])):
+        if "us" in r:
+            out.append("| %d | %d | %.1f | %.1f |" % (r["grid"], r["two_tiles"], r["us"], r["tflops"]))
+        else:
+            out.append("| %d | %d | refused | - |" % (r["grid"], r["two_tiles"]))
+    return "\n".join(out) + "\n"
 
 
 def summarize_shapes(rows):
@@ -230,6 +294,10 @@ def main():
                     help="paired bursts; BASE and VARIANT are JSON option dicts, e.g. "
                          "'{\"schedule\": \"persistent\"}' '{\"schedule\": \"streamk\"}'")
     ap.add_argument("--layout-b", type=int, default=1, help="0 row-major, 1 column-major B")
+    ap.add_argument("--skinny", action="store_true",
+                    help="time SKINNY_SHAPES (fp16, row-major A and B)")
+    ap.add_argument("--out", help="also write every record to this file as JSON lines")
+    ap.add_argument("--markdown", help="write the sweeps as markdown tables to this file")
     args = ap.parse_args()
     dtype = B.GEMM_BF16 if args.dtype == "bf16" else B.GEMM_F16
     B.load()
@@ -237,15 +305,38 @@ def main():
         M, N, K = (int(x) for x in args.compare[:3])
         print(json.dumps(paired_compare(M, N, K, json.loads(args.compare[3]), json.loads(args.compare[4]),
                                         dtype=dtype, lb=args.layout_b)), flush=True)
+    records, md = [], []
+
+    def emit(rec):
+        records.append(rec)
+        print(json.dumps(rec), flush=True)
+
     if args.grid_sweep:
-        for row in grid_sweep(*args.grid_sweep, dtype=dtype):
-            print(json.dumps(row), flush=True)
+        rows = grid_sweep(*args.grid_sweep, dtype=dtype)
+        for row in rows:
+            emit(row)
+        md.append(grid_markdown(rows))
     if args.shapes or args.large:
-        rows = shape_sweep(args.shapes, dtype=dtype, max_macs=args.max_macs,
+        rows = shape_sweep(args.shapes, dtype=dtype, max_macs=args.max_macs, lb=args.layout_b,
                            extra_shapes=LARGE_SHAPES if args.large else ())
         for row in rows:
-            print(json.dumps(row), flush=True)
-        print(json.dumps({"summary": summarize_shapes(rows)}), flush=True)
+            emit(row)
+        emit({"summary": summarize_shapes(rows)})
+        md.append(markdown(rows, "Log-sampled and large shapes, %s, A row-major, B %s-major"
+                           % (args.dtype, "column" if args.layout_b else "row")))
+    if args.skinny:
+        rows = shape_sweep(0, dtype=B.GEMM_F16, la=0, lb=0, extra_shapes=SKINNY_SHAPES)
+        for row in rows:
+            emit(row)
+        emit({"summary_skinny": summarize_shapes(rows)})
+        md.append(markdown(rows, "Single row of tiles (skinny), fp16, A and B row-major"))
+    if args.out:
+        with open(args.out, "w") as f:
+            for rec in records:
+                f.write(json.dumps(rec) + "\n")
+    if args.markdown:
+        with open(args.markdown, "w") as f:
+            f.write("\n".join(m for m in md if m))
 
 
 if __name__ == "__main__":

@@ -167,8 +167,9 @@ def test_auto_schedule_choices(lib):
         # from the timed sweep of log-sampled shapes
         (3840, 2816, 5888): (B.GEMM_SCHED_STREAMK, 0),
         (768, 6656, 2304): (B.GEMM_SCHED_STREAMK, 1),
-        (4352, 512, 5888): (B.GEMM_SCHED_PERSISTENT, 0),
-        (256, 1792, 6400): (B.GEMM_SCHED_STREAMK, 1),
+        (4352, 512, 5888): (B.GEMM_SCHED_SPLITK, 0),     # cluster split-K fits one wave
+        (256, 1792, 6400): (B.GEMM_SCHED_SPLITK, 0),
+        (512, 2048, 768): (B.GEMM_SCHED_PERSISTENT, 0),  # fits, but parts of 6 k-blocks
         (512, 5632, 1280): (B.GEMM_SCHED_STREAMK, 1),
         (4608, 5120, 1024): (B.GEMM_SCHED_PERSISTENT, 0),
         # four or more waves: hybrid for long tiles or many waves
@@ -179,7 +180,7 @@ def test_auto_schedule_choices(lib):
     for (M, N, K), (sched, mode) in cases.items():
         p = B.Plan(M, N, K, B.GEMM_BF16, 0, 1, "auto", offline_sms=152)
         assert (p.info("schedule"), p.info("sk_mode")) == (sched, mode), (M, N, K)
-        assert p.info("split_k_cluster") == (1 if M <= 128 else 0), (M, N, K)
+        assert p.info("split_k_cluster") == (1 if sched == B.GEMM_SCHED_SPLITK else 0), (M, N, K)
         p.close()
 
 

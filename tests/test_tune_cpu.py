@@ -51,3 +51,20 @@ def test_paired_compare_alternates_and_reports_the_paired_ratio(monkeypatch):
     assert timed == ["persistent", "streamk", "streamk", "persistent"] * 2
     assert all(c[1] == {"group_m": 8} for c in calls if c[0] == "persistent")
     assert r["launches"] == int(20.0 * 1e3 / 100.0)
+
+
+def test_markdown_tables_and_auto_choice():
+    rows = [{"M": 64, "N": 8192, "K": 8192, "results": {
+                "streamk": {"tflops": 260.0}, "splitk_cluster": {"tflops": 300.0},
+                "auto": {"tflops": 299.0, "schedule": 3, "split_k_cluster": 1, "sk_mode": 0}}},
+            {"M": 8192, "N": 8192, "K": 8192, "results": {
+                "streamk": {"tflops": 1600.0}, "splitk_cluster": {"refused": "x"},
+                "auto": {"tflops": 1600.0, "schedule": 2, "split_k_cluster": 0, "sk_mode": 1}}}]
+    md = tune.markdown(rows, "t")
+    assert "| 64 | 8192 | 8192 | 260.0 | **300.0** | 299.0 (splitk_cluster) | 0.997 |" in md
+    assert "| 8192 | 8192 | 8192 | **1600.0** | - | 1600.0 (streamk_all) | 1.000 |" in md
+    assert "- auto:" in md
+    g = tune.grid_markdown([{"M": 1, "N": 2, "K": 3, "grid": 152, "two_tiles": 1, "us": 10.0, "tflops": 1.5},
+                            {"M": 1, "N": 2, "K": 3, "grid": 300, "two_tiles": 0, "refused": "no"}])
+    assert "| 152 | 1 | 10.0 | 1.5 |" in g and "| 300 | 0 | refused | - |" in g
+    assert len(tune.SKINNY_SHAPES) == 45 and all(m <= 128 for m, _, _ in tune.SKINNY_SHAPES)
