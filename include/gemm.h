@@ -181,7 +181,16 @@ enum {
      * tiles x S CTAs.  A split of K reduced inside a cluster has
      * no counterpart on the pages (the issue's closing comments name split-K
      * only). */
-    GEMM_OPT_SPLIT_K_CLUSTER = 16
+    GEMM_OPT_SPLIT_K_CLUSTER = 16,
+    /* k-blocks of A and B of each CTA's first unit prefetched into L2 before
+     * the launch waits for the previous kernel in the stream: 0 = off, up to
+     * 256; -1 (default) = 8 when the launch fills at least three quarters of
+     * the SMs, else 0 (GEMM_INFO_EARLY_PREFETCH reports the value used).  A CTA
+     * that starts while the previous kernel drains uses that kernel's tail to
+     * fetch its first operands.  Only L2 is filled (the point of coherence),
+     * so results are unchanged whatever the previous kernel wrote.  No
+     * counterpart on the pages. */
+    GEMM_OPT_EARLY_PREFETCH = 17
 };
 
 /* Keys for gemm_plan_get_info. */
@@ -211,8 +220,9 @@ enum {
     GEMM_INFO_HOST_CHUNKS = 25,     /* row chunks of gemm_run_host's block grid */
     GEMM_INFO_HOST_COL_CHUNKS = 26, /* column chunks (both 1: serial) */
     GEMM_INFO_SPLIT_K_CLUSTER = 27, /* 1 when split-K parts reduce inside a cluster */
-    GEMM_INFO_CLUSTERS_RESIDENT = 28 /* clusters of this plan's kernel that fit the GPU at
+    GEMM_INFO_CLUSTERS_RESIDENT = 28,/* clusters of this plan's kernel that fit the GPU at
                                         once (0: no clusters, or an offline plan) */
+    GEMM_INFO_EARLY_PREFETCH = 29   /* k-blocks prefetched into L2 before the grid wait */
 };
 
 /* Roles of a work unit reported by gemm_plan_units.  CLUSTER_PART: one k-part

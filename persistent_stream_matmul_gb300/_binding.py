@@ -39,6 +39,7 @@ GEMM_OPT_RASTER = 13
 GEMM_OPT_HOST_CHUNKS = 14
 GEMM_OPT_HOST_COL_CHUNKS = 15
 GEMM_OPT_SPLIT_K_CLUSTER = 16
+GEMM_OPT_EARLY_PREFETCH = 17
 
 INFO = {
     "tile_m": 1, "tile_n": 2, "tile_k": 3, "tiles_m": 4, "tiles_n": 5, "tiles": 6,
@@ -46,7 +47,7 @@ INFO = {
     "sk_iters_rem": 11, "num_sms": 12, "stages": 13, "group_m": 14, "smem_bytes": 15, "cluster_m": 16,
     "a_rows_per_stage": 17, "split_k": 18, "k_rotate": 19,
     "l2_prefetch": 20, "pair_mma": 21, "schedule": 22, "sk_mode": 23, "raster": 24, "host_chunks": 25, "host_col_chunks": 26,
-    "split_k_cluster": 27, "clusters_resident": 28,
+    "split_k_cluster": 27, "clusters_resident": 28, "early_prefetch": 29,
 }
 ROLE_FULL, ROLE_OWNER, ROLE_PEER, ROLE_CLUSTER_PART = 0, 1, 2, 3
 TRACE_STAMPS = 6   # uint64 per CTA written by gemm_plan_set_trace: 4 timer + 2 clock stamps
@@ -226,7 +227,7 @@ class Plan:
                 "k_rotate": GEMM_OPT_K_ROTATE, "l2_prefetch": GEMM_OPT_L2_PREFETCH,
                 "pair_mma": GEMM_OPT_PAIR_MMA, "raster": GEMM_OPT_RASTER,
                 "host_chunks": GEMM_OPT_HOST_CHUNKS, "host_col_chunks": GEMM_OPT_HOST_COL_CHUNKS,
-                "split_cluster": GEMM_OPT_SPLIT_K_CLUSTER}
+                "split_cluster": GEMM_OPT_SPLIT_K_CLUSTER, "early_prefetch": GEMM_OPT_EARLY_PREFETCH}
         for k, v in options.items():
             if v is not None:
                 gemm_plan_set_option(self.handle, keys[k], int(v))

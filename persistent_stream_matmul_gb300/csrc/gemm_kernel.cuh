@@ -111,6 +111,7 @@ struct KParams {
     uint64_t wait_limit_ns;      // owner's wait for its peers
     uint64_t pipe_limit_ns;      // any wait inside the CTA's own pipeline
     unsigned long long* trace;   // optional: TRACE_N stamps per CTA, or null
+    int32_t early_prefetch;      // k-blocks of the first unit brought into L2 before the wait
 };
 
 // Per-CTA trace stamps: nanoseconds of %globaltimer at the start of the CTA,
@@ -320,6 +321,37 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // Everything above touches only this CTA's shared and tensor memory, so
     // it may overlap the previous kernel in the stream; global memory (A, B,
     // C, workspace, status) is touched only after that kernel has finished.
+    // The one exception is an L2 prefetch of the operands of this CTA's first
+    // unit (GEMM_OPT_EARLY_PREFETCH): it brings lines into L2 without
+    // reading them into the CTA, and L2 is the point of coherence, so a write
+    // by the previous kernel to the same lines still lands before any read
+    // made after the wait.  It uses the DRAM time of the previous kernel's
+    // tail, for the CTAs that start on SMs that kernel left idle.
+    if (p.early_prefetch > 0 && warp == 0 && lane == 0) {
+        Cursor cur;
+        cursor_init(p.s, unit_cta, cur);
+        Unit u;
+        if (cursor_next(p.s, unit_cta, cur, u)) {
+            const int m0 = (u.tm * CM + rank) * BM, n0 = u.tn * BN;
+            const int nk = min(u.k1 - u.k0, p.early_prefetch);
+            for (int i = 0; i < nk; ++i) {
+                const int k_el = unit_kblock(p.s, u.tile, u.k0, u.k1, i) * BK;
+                if (!p.b_mn) {
+                    tma_prefetch_l2_2d(&tmB, k_el, n0 + rank * (BN / CM));
+                } else {
+#pragma unroll 1
+                    for (int c = rank * (BN / 64) / CM; c < (rank + 1) * (BN / 64) / CM; ++c)
+                        tma_prefetch_l2_2d(&tmB, n0 + 64 * c, k_el);
+                }
+                if (!p.a_mn) {
+                    tma_prefetch_l2_2d(&tmA, k_el, m0);
+                } else {
+#pragma unroll 1
+                    for (int c = 0; c < AROWS / 64; ++c) tma_prefetch_l2_2d(&tmA, m0 + 64 * c, k_el);
+                }
+            }
+        }
+    }
     grid_dependency_wait();
     if (threadIdx.x == 0) {
         grid_launch_dependents();

@@ -424,3 +424,24 @@ def test_cluster_splitk_defaults_and_refusals(lib):
     p = B.Plan(64, 8192, 8192, B.GEMM_F16, 0, 0, "streamk", offline_sms=152, split_cluster=1)
     assert p.info("split_k_cluster") == 0 and p.workspace_size > 0
     p.close()
+
+
+def test_early_prefetch_default_and_option(lib):
+    # 8 k-blocks when the launch fills at least 3/4 of the SMs, else none
+    for shape, want in (((64, 8192, 8192), 8), ((16, 1024, 4096), 0), ((8192, 8192, 8192), 8),
+                        ((2304, 2304, 8192), 8), ((512, 512, 512), 0)):
+        p = B.Plan(*shape, B.GEMM_F16, 0, 0, "auto", offline_sms=152)
+        ctas = p.info("grid")
+        assert p.info("early_prefetch") == want == (8 if 4 * ctas >= 3 * 152 else 0), shape
+        p.close()
+    p = B.Plan(64, 8192, 8192, B.GEMM_F16, 0, 0, "auto", offline_sms=152, early_prefetch=3)
+    assert p.info("early_prefetch") == 3
+    p.set_option(B.GEMM_OPT_EARLY_PREFETCH, 0)
+    assert p.info("early_prefetch") == 0
+    p.set_option(B.GEMM_OPT_EARLY_PREFETCH, -1)
+    assert p.info("early_prefetch") == 8
+    for bad in (-2, 257):
+        with pytest.raises(B.GemmError) as e:
+            p.set_option(B.GEMM_OPT_EARLY_PREFETCH, bad)
+        assert e.value.status == B.GEMM_ERR_UNSUPPORTED
+    p.close()

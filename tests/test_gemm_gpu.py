@@ -481,3 +481,51 @@ def test_run_host_end_to_end():
     Cb = hC.numpy().view(np.uint16).reshape(M, N)
     _check_full(Cb, A, Bm, M, N, K, dtype, 0, 1)
     p.close()
+
+
+@pytest.mark.parametrize("sched", ["streamk", "splitk", "persistent"])
+def test_chained_products_read_the_previous_output(sched):
+    # C1 = A1 B1, then at once C2 = A2 C1 in the same stream: the second launch
+    # starts while the first drains (programmatic dependent launch) and
+    # prefetches its operands into L2 before waiting for it, yet it must read
+    # the C1 that the first product wrote.  Integer inputs keep C2 exact: C1
+    # holds integers, and every partial sum of C2 stays below 2^24.
+    M1, N1, K1, dt = 512, 1024, 2048, inputs.BF16
+    M2 = 384
+    ws = Workspace()
+    p1 = B.Plan(M1, N1, K1, dt, 0, 1, "streamk")
+    p2 = B.Plan(M2, N1, M1, dt, 0, 0, sched, early_prefetch=8)
+    stream = torch.cuda.current_stream()
+    for rep in range(3):
+        A1, B1 = inputs.operands(M1, N1, K1, dt, 0, 1, inputs.INT_LAW, inputs.INT_LAW, 90 + rep)
+        A2 = inputs.matrix(M2, M1, 0, dt, inputs.INT_LAW, 95 + rep, 1)
+        dA1, dB1, dA2 = to_device(A1), to_device(B1), to_device(A2)
+        C1 = torch.empty(M1 * N1, dtype=torch.int16, device="cuda")
+        C2 = torch.empty(M2 * N1, dtype=torch.int16, device="cuda")
+        w1 = ws.get(p1.workspace_size)
+        w2 = torch.zeros(max(1, p2.workspace_size), dtype=torch.uint8, device="cuda")
+        p1.run(dA1, dB1, C1, w1, stream)
+        p2.run(dA2, C1, C2, w2 if p2.workspace_size else None, stream)
+        assert p2.last_status(stream) == B.GEMM_OK and p1.last_status(stream) == B.GEMM_OK
+        c1 = C1.cpu().numpy().view(np.uint16).reshape(M1, N1)
+        _, _, ref1 = oracle.gemm(A1, B1, M1, N1, K1, dt, 0, 1, with_abs=False)
+        assert np.array_equal(c1, ref1)
+        _, _, ref2 = oracle.gemm(A2, c1, M2, N1, M1, dt, 0, 0, with_abs=False)
+        assert np.array_equal(C2.cpu().numpy().view(np.uint16).reshape(M2, N1), ref2), rep
+    p1.close()
+    p2.close()
+
+
+@pytest.mark.parametrize("sched,opts", [("streamk", {}), ("streamk", {"sk_mode": 1}), ("dp", {}),
+                                        ("splitk", {"split_cluster": 1})])
+def test_early_prefetch_changes_no_bit(sched, opts):
+    M, N, K, dt = 1024, 1536, 4096, inputs.BF16
+    A, Bm, dA, dB = _case(M, N, K, dt, 0, 1, ("normal", 1.0), 23)
+    ws = Workspace()
+    outs = []
+    for d in (0, 8, 64):
+        p = B.Plan(M, N, K, dt, 0, 1, sched, early_prefetch=d, **opts)
+        outs.append(run(p, dA, dB, M, N, ws))
+        p.close()
+    assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[0], outs[2])
+    _check_full(outs[0], A, Bm, M, N, K, dt, 0, 1)
