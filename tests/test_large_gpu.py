@@ -1,12 +1,13 @@
 """GPU parity at large sizes: a tall product, a very deep K on a small output
-(long Stream-K and split-K ranges), and a wide N; sampled entries against the
-oracle, integer-valued operands bit-exact."""
+(long Stream-K and split-K ranges, eight 32768-deep parts of cluster split-K),
+and a wide N (cluster split-K in waves of 2-CTA clusters); sampled entries
+against the oracle, integer-valued operands bit-exact."""
 import numpy as np
 import pytest
 
 import oracle
 from persistent_stream_matmul_gb300 import _binding as B
-from persistent_stream_matmul_gb300 import inputs
+from persistent_stream_matmul_gb300 import inputs, tune
 from tests.gpu_util import Workspace, ensure_built, run, to_device
 
 pytestmark = pytest.mark.gpu
@@ -14,8 +15,8 @@ pytestmark = pytest.mark.gpu
 CASES = [
     # M, N, K, dtype, layout A, layout B, schedules
     (16384, 2048, 4096, inputs.BF16, 0, 1, ("persistent", "streamk", "auto")),
-    (256, 256, 262144, inputs.BF16, 0, 1, ("streamk", "splitk", "auto")),
-    (128, 65536, 1024, inputs.F16, 0, 0, ("dp", "streamk", "auto")),
+    (256, 256, 262144, inputs.BF16, 0, 1, ("streamk", "splitk", "splitk_cluster", "auto")),
+    (128, 65536, 1024, inputs.F16, 0, 0, ("dp", "streamk", "splitk_cluster", "auto")),
 ]
 
 
@@ -37,7 +38,8 @@ def test_large(M, N, K, dtype, la, lb, scheds):
         C64, S = oracle.gemm_entries(A, Bm, M, N, K, dtype, la, lb, rows, cols)
         ref = oracle.round_to(C64, dtype)
         for sched in scheds:
-            p = B.Plan(M, N, K, dtype, la, lb, sched)
+            kind, opts = tune.SCHEDULE_VARIANTS[sched]
+            p = B.Plan(M, N, K, dtype, la, lb, kind, **opts)
             got = run(p, dA, dB, M, N, ws)[rows, cols]
             p.close()
             ok, worst, nbad = oracle.check(got, dtype, C64, S, K)
