@@ -93,7 +93,7 @@ struct Cfg {
     static_assert(AROWS == 128 || AROWS == 64, "rows of A per stage");
     static_assert(AROWS == 128 || A_STAGE_BYTES + B_STAGE_BYTES >= BM * BK * 2,
                   "the MMA's 128-row read of A must stay inside the stage");
-    static_assert((2 * STAGES + 6) * 8 + 8 <= BAR_BYTES, "barrier area");
+    static_assert((2 * STAGES + 7) * 8 + 8 <= BAR_BYTES, "barrier area");
 };
 
 struct KParams {
@@ -226,6 +226,125 @@ __device__ __forceinline__ void cluster_reduce_slice(uint32_t sbase, int part, i
     }
 }
 
+// Cluster split-K exchange by bulk copies, when the ring holds both a staged
+// partial and the slots for the other parts (2 * AROWS * BN * 4 bytes).  CTA
+// `part` owns columns [part * BN / KC, (part + 1) * BN / KC) of the tile.
+//  1. Its ring is idle (this accumulator is ready): tell the other CTAs they
+//     may copy into it, and arm this CTA's receive barrier for their bytes.
+//  2. Stage the partial slice by slice (slice q at q * SLOT: row r at
+//     r * W * 4, 16-byte units XOR-swizzled by row), so each slice is one
+//     contiguous block.
+//  3. Once the other CTAs may be written, one thread bulk-copies each
+//     foreign slice into its owner's slot for this part (the copy engine,
+//     completing on the owner's barrier in bytes).
+//  4. Wait for this CTA's slots, then sum its slice in ascending part (= k)
+//     order, ((P0 + P1) + P2) + ..., in fp32, round once and store C.
+// Every wait is bounded; one that runs out records a timeout and the CTA
+// stores nothing.  skip_copies (test hook) withholds step 3.
+template <int KC, int BN, int AROWS, bool OUT_BF16>
+__device__ __forceinline__ void cluster_exchange_bulk(uint32_t ring, uint32_t free_bar, uint32_t recv_bar,
+                                                      int part, uint32_t tbase, int row, bool row_ok,
+                                                      int rows, int et, bool empty, bool skip_copies,
+                                                      uint64_t limit_ns, int* status, uint8_t* ctile,
+                                                      int ldc, int col0, int N) {
+    constexpr int W = BN / KC;                   // columns of a slice
+    constexpr int U = W / 4;                     // 16-byte units in a slice row
+    constexpr int SW = (U < 8 ? U : 8) - 1;      // swizzle mask
+    constexpr uint32_t SLOT = (uint32_t)AROWS * W * 4;
+    constexpr uint32_t RECV = (uint32_t)KC * SLOT;  // slots after the staged partial
+    static_assert(U >= 4 && (U & (U - 1)) == 0, "slice rows of 4, 8, 16 or 32 units");
+    const uint32_t bytes = (uint32_t)rows * W * 4;  // a slice's valid rows, a multiple of 16
+    // 1. this ring is free: the other parts may copy into its slots
+    fence_proxy_async_smem();  // the ring was last used by the async proxy
+    named_bar_sync(BAR_EPI_SYNC, EPI_THREADS);
+    if (et == 0) {
+        mbar_arrive_expect_tx(recv_bar, (uint32_t)(KC - 1) * bytes);
+#pragma unroll
+        for (int q = 0; q < KC; ++q)
+            if (q != part) mbar_arrive_cluster(mapa_shared(free_bar, (uint32_t)q));
+    }
+    // 2. stage the partial, slice by slice
+#pragma unroll 1
+    for (int j = 0; j < BN / 32; ++j) {
+        uint32_t r[32];
+        __syncwarp();
+        tmem_ld_32x32b_x32(tbase + j * 32, r);
+        if (row_ok) {
+#pragma unroll
+            for (int v = 0; v < 8; ++v) {
+                const int gu = j * 8 + v;
+                const int q = gu / U, u = gu % U;
+                st_shared_u4(ring + (uint32_t)q * SLOT + (uint32_t)row * (W * 4) + (uint32_t)((u ^ (row & SW)) * 16),
+                             empty ? 0u : r[4 * v], empty ? 0u : r[4 * v + 1], empty ? 0u : r[4 * v + 2],
+                             empty ? 0u : r[4 * v + 3]);
+            }
+        }
+    }
+    fence_proxy_async_smem();  // the staged bytes, for the copy engine
+    named_bar_sync(BAR_EPI_SYNC, EPI_THREADS);
+    // 3. copy the foreign slices once their owners may be written
+    bool sent = false;
+    if (et == 0) {
+        const bool may = mbar_wait_acq_cluster(free_bar, 0, limit_ns);
+        if (!may) record_status(status, STATUS_FLAG_TIMEOUT);
+        if (may && !skip_copies) {
+#pragma unroll
+            for (int q = 0; q < KC; ++q)
+                if (q != part)
+                    bulk_copy_to_cluster(mapa_shared(ring + RECV + (uint32_t)part * SLOT, (uint32_t)q),
+                                         ring + (uint32_t)q * SLOT, bytes,
+                                         mapa_shared(recv_bar, (uint32_t)q));
+            bulk_commit_group();
+            sent = true;
+        }
+    }
+    // 4. this CTA's slots, then its slice
+    const bool got = epi_vote_all(mbar_wait_acq_cluster(recv_bar, 0, limit_ns));
+    if (!got) {
+        if (et == 0) record_status(status, STATUS_FLAG_TIMEOUT);
+    } else {
+        constexpr int BATCH = 16 / KC;
+        const int total = rows * U;
+#pragma unroll 1
+        for (int base = et; base < total; base += EPI_THREADS * BATCH) {
+            float4 x[BATCH][KC];
+#pragma unroll
+            for (int b = 0; b < BATCH; ++b) {
+                const int idx = base + b * EPI_THREADS;
+                if (idx < total) {
+                    const int rr = idx / U, u = idx % U;
+                    const uint32_t off = (uint32_t)rr * (W * 4) + (uint32_t)((u ^ (rr & SW)) * 16);
+#pragma unroll
+                    for (int s = 0; s < KC; ++s)
+                        x[b][s] = ld_shared_f4(s == part ? ring + (uint32_t)part * SLOT + off
+                                                         : ring + RECV + (uint32_t)s * SLOT + off);
+                }
+            }
+#pragma unroll
+            for (int b = 0; b < BATCH; ++b) {
+                const int idx = base + b * EPI_THREADS;
+                if (idx < total) {
+                    const int rr = idx / U;
+                    const int col = col0 + (part * U + idx % U) * 4;
+                    float4 acc = x[b][0];
+#pragma unroll
+                    for (int s = 1; s < KC; ++s) {
+                        acc.x += x[b][s].x;
+                        acc.y += x[b][s].y;
+                        acc.z += x[b][s].z;
+                        acc.w += x[b][s].w;
+                    }
+                    if (col < N)
+                        st_u2(ctile + ((size_t)rr * ldc + col) * 2, pack2<OUT_BF16>(acc.x, acc.y),
+                              pack2<OUT_BF16>(acc.z, acc.w));
+                }
+            }
+        }
+    }
+    // the copies out of this CTA's ring have landed before it may be released
+    if (sent) bulk_wait_group_0();
+}
+
 template <bool OUT_BF16>
 __device__ __forceinline__ uint32_t pack2(float a, float b) {
     if constexpr (OUT_BF16) {
@@ -264,9 +383,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     auto tfull_bar = [&](int b) { return bar_base + 8u * (2 * STAGES + b); };
     auto tempty_bar = [&](int b) { return bar_base + 8u * (2 * STAGES + 2 + b); };
     const uint32_t done_bar = bar_base + 8u * (2 * STAGES + 4);
-    const uint32_t parts_bar = bar_base + 8u * (2 * STAGES + 5);  // cluster split-K
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_area + 8 * (2 * STAGES + 6));
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(bar_area + 8 * (2 * STAGES + 6) + 4);
+    // cluster split-K: the other parts' signals, and the bytes of their slices
+    const uint32_t parts_bar = bar_base + 8u * (2 * STAGES + 5);
+    const uint32_t recv_bar = bar_base + 8u * (2 * STAGES + 6);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_area + 8 * (2 * STAGES + 7));
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(bar_area + 8 * (2 * STAGES + 7) + 4);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -290,7 +411,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         mbar_init(done_bar, 1);
         // one release-arrive from each other CTA of the cluster
-        if constexpr (KCL) mbar_init(parts_bar, (uint32_t)(p.s.kc > 1 ? p.s.kc - 1 : 1));
+        if constexpr (KCL) {
+            mbar_init(parts_bar, (uint32_t)(p.s.kc > 1 ? p.s.kc - 1 : 1));
+            mbar_init(recv_bar, 1);
+        }
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -577,7 +701,40 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const int row = tm * BM + row_in_tile;
             const bool row_ok = row_in_tile < rows_valid;
 
-            if constexpr (KCL) {
+            if constexpr (KCL && AROWS == 64) {
+                // every unit of a cluster split-K plan is a CLUSTER_PART, and
+                // the CTA's only unit.  With half-height A stages (M <= 64) the
+                // ring holds the staged partial and the slots for the other
+                // parts: exchange by bulk copies.  (Paired bursts: 1.3 % faster
+                // on 64 x 8192 x 8192 and 3.9 % on 16 x 1024 x 16384 than the
+                // pull below; on 128 x 4096 x 4096, with full-height tiles,
+                // 1.8 % slower, so full-height tiles keep the pull.)
+                static_assert(2u * AROWS * BN * 4 <= (uint32_t)STAGES * Cf::STAGE_BYTES,
+                              "the staged partial and the slots fit the ring");
+                const int part = (int)cluster_ctarank();  // = u.slot: CTA c is part c mod kc
+                const bool empty = u.k1 <= u.k0;
+                const bool skip = cta == p.inject_skip_cta;
+                uint8_t* ctile = reinterpret_cast<uint8_t*>(p.C) + (size_t)tm * BM * p.ldc * 2;
+                const int col0 = u.tn * BN;
+                if (p.s.kc == 2)
+                    cluster_exchange_bulk<2, BN, AROWS, OUT_BF16>(sbase, parts_bar, recv_bar, part, tbase,
+                                                                  row_in_tile, row_ok, rows_valid, et, empty,
+                                                                  skip, p.wait_limit_ns, p.status, ctile,
+                                                                  p.ldc, col0, p.N);
+                else if (p.s.kc == 4)
+                    cluster_exchange_bulk<4, BN, AROWS, OUT_BF16>(sbase, parts_bar, recv_bar, part, tbase,
+                                                                  row_in_tile, row_ok, rows_valid, et, empty,
+                                                                  skip, p.wait_limit_ns, p.status, ctile,
+                                                                  p.ldc, col0, p.N);
+                else
+                    cluster_exchange_bulk<8, BN, AROWS, OUT_BF16>(sbase, parts_bar, recv_bar, part, tbase,
+                                                                  row_in_tile, row_ok, rows_valid, et, empty,
+                                                                  skip, p.wait_limit_ns, p.status, ctile,
+                                                                  p.ldc, col0, p.N);
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(tempty_bar(buf));
+            } else if constexpr (KCL) {
                 // every unit of a cluster split-K plan is a CLUSTER_PART
                 // The CTA's only unit: its ring is idle (every copy has landed
                 // and every MMA that read it has completed once this
