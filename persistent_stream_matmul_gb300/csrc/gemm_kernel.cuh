@@ -619,12 +619,30 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             int stage = 0;
             uint32_t phase = 0, iter = 0;
             bool ok = true;
+            // Descriptors of stage 0's A and B tiles and the step of one
+            // 16-element k-slice, computed once: the loop below only adds
+            // offsets (the 14-bit address field cannot carry, the shared
+            // window is below 256 KB).  The issue loop must stay lean: with
+            // the descriptors rebuilt from kernel parameters for every MMA
+            // (and reloaded after each one, the MMA asm clobbering memory),
+            // and the abort flag read every k-block, the tensor pipe idled
+            // ~10 % of the time even with no copies to wait for.
+            //   K-major: a k-slice is 32 bytes along the swizzled row.
+            //   MN-major: 16 k-rows of 128 bytes.
+            const uint64_t a_desc0 =
+                smem_desc_sw128(sbase, p.a_mn ? MN_CHUNK_BYTES : 16, SW_ATOM_BYTES);
+            const uint64_t b_desc0 =
+                smem_desc_sw128(sbase + Cf::A_STAGE_BYTES, p.b_mn ? MN_CHUNK_BYTES : 16, SW_ATOM_BYTES);
+            const uint64_t a_kstep = p.a_mn ? (16 * 128) >> 4 : (UMMA_K * 2) >> 4;
+            const uint64_t b_kstep = p.b_mn ? (16 * 128) >> 4 : (UMMA_K * 2) >> 4;
+            const uint32_t idesc = p.idesc;
             while (ok && cursor_next(p.s, unit_cta, cur, u)) {
                 const int buf = iter & 1;
                 if (!mbar_wait(tempty_bar(buf), ((iter >> 1) & 1u) ^ 1u, p.pipe_limit_ns)) {
                     fail_pipe();
                     break;
                 }
+                if (*abort_flag) break;
                 tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + (uint32_t)(buf * BN);
                 for (int i = 0; i < u.k1 - u.k0; ++i) {
@@ -633,24 +651,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         ok = false;
                         break;
                     }
-                    if (*abort_flag) { ok = false; break; }
                     tc_fence_after_sync();
-                    const uint32_t sa = sbase + stage * Cf::STAGE_BYTES;
-                    const uint32_t sb = sa + Cf::A_STAGE_BYTES;
+                    const uint64_t off = (uint64_t)((uint32_t)(stage * Cf::STAGE_BYTES) >> 4);
 #pragma unroll
                     for (int kk = 0; kk < BK / UMMA_K; ++kk) {
-                        // K-major: a k-step of 16 elements is 32 bytes along the
-                        // swizzled row.  MN-major: 16 k-rows of 128 bytes.
-                        const uint64_t adesc =
-                            p.a_mn ? smem_desc_sw128(sa + kk * 16 * 128, MN_CHUNK_BYTES, SW_ATOM_BYTES)
-                                   : smem_desc_sw128(sa + kk * UMMA_K * 2, 16, SW_ATOM_BYTES);
-                        const uint64_t bdesc =
-                            p.b_mn ? smem_desc_sw128(sb + kk * 16 * 128, MN_CHUNK_BYTES, SW_ATOM_BYTES)
-                                   : smem_desc_sw128(sb + kk * UMMA_K * 2, 16, SW_ATOM_BYTES);
+                        const uint64_t adesc = a_desc0 + off + (uint64_t)kk * a_kstep;
+                        const uint64_t bdesc = b_desc0 + off + (uint64_t)kk * b_kstep;
                         if constexpr (PAIR_MMA)
-                            mma_f16_ss_pair(d_tmem, adesc, bdesc, p.idesc, (i > 0 || kk > 0) ? 1u : 0u);
+                            mma_f16_ss_pair(d_tmem, adesc, bdesc, idesc, (i > 0 || kk > 0) ? 1u : 0u);
                         else
-                            mma_f16_ss(d_tmem, adesc, bdesc, p.idesc, (i > 0 || kk > 0) ? 1u : 0u);
+                            mma_f16_ss(d_tmem, adesc, bdesc, idesc, (i > 0 || kk > 0) ? 1u : 0u);
                     }
                     if constexpr (PAIR_MMA) {
                         mma_commit_pair_multicast(empty_bar(stage), PAIR_MASK);  // frees both rings

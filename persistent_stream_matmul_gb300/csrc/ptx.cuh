@@ -258,15 +258,17 @@ __device__ __forceinline__ void tc_fence_after_sync() {
 }
 
 // D[tmem] (+)= A[smem] * B[smem], fp16/bf16 inputs, fp32 accumulator.
-// accumulate == 0 overwrites D.
+// accumulate == 0 overwrites D.  No "memory" clobber: the MMA touches no
+// memory the compiler tracks, and volatile asm keeps its order relative to
+// the barrier waits and fences around it; a clobber would make the compiler
+// reload loop state from memory between the MMAs of a k-block.
 __device__ __forceinline__ void mma_f16_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                            uint32_t idesc, uint32_t accumulate) {
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate));
 }
 
 // Pair MMA, issued by one thread of the pair's first CTA: D (256 x N, rows
@@ -279,8 +281,7 @@ __device__ __forceinline__ void mma_f16_ss_pair(uint32_t d_tmem, uint64_t a_desc
         "{\n\t.reg .pred p;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate));
 }
 
 // Arrive once on the mbarrier at `bar`'s offset in every CTA of cta_mask when
