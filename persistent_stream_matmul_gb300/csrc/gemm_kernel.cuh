@@ -69,6 +69,11 @@ constexpr int MN_CHUNK_BYTES = 64 * BK * 2;  // one 64-element-wide MN-major box
 enum : int { STATUS_OK = 0, STATUS_FLAG_TIMEOUT = 1, STATUS_PIPE_TIMEOUT = 2 };
 enum : uint32_t { BAR_EPI_SYNC = 1, BAR_EPI_VOTE = 2 };  // named barriers (0 = __syncthreads)
 
+template <bool V>
+struct BoolConst {
+    static constexpr bool value = V;
+};
+
 // AROWS: rows of A loaded per stage.  128 normally.  64 when M <= 64: the
 // MMA still reads 128 rows, and rows 64-127 alias the first bytes of the
 // stage's B tile, so those accumulator rows hold garbage that is never stored
@@ -495,6 +500,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (lane == 0) {
             // With a single row of tiles every B tile is read exactly once:
             // let it leave L2 first and keep the small, shared A resident.
+            // Otherwise the copies carry no L2 policy at all (the cache-hint
+            // form measured ~1.5 % slower on a large square product).  The
+            // choice is a compile-time constant of the loop below: a run-time
+            // branch between the two copy forms made that loop ~7 % slower.
             const bool b_once = p.s.tiles_m == 1;
             const uint64_t pol_a = b_once ? l2_policy_evict_last() : l2_policy_evict_normal();
             const uint64_t policy = b_once ? l2_policy_evict_first() : l2_policy_evict_normal();
@@ -505,97 +514,105 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             uint32_t phase = 0;
             uint32_t filled = 0, fill_parity = 0;  // per-stage bit masks
             bool ok = true;
-            while (ok && cursor_next(p.s, unit_cta, cur, u)) {
-                const int m0 = (u.tm * CM + rank) * BM, n0 = u.tn * BN;
-                const int nk = u.k1 - u.k0;
-                // L2 prefetch of B, l2_prefetch k-blocks ahead of the loads: keeps
-                // DRAM busy beyond what the shared-memory ring can hold in flight
-                const int pf = p.s.l2_prefetch;
-                auto prefetch_b = [&](int step) {
-                    const int kp = unit_kblock(p.s, u.tile, u.k0, u.k1, step) * BK;
-                    if (!p.b_mn) {
-                        tma_prefetch_l2_2d(&tmB, kp, n0 + rank * (BN / CM));
-                    } else {
+            auto produce = [&](auto hint_tag) {
+                constexpr bool HINT = decltype(hint_tag)::value;
+                while (ok && cursor_next(p.s, unit_cta, cur, u)) {
+                    const int m0 = (u.tm * CM + rank) * BM, n0 = u.tn * BN;
+                    const int nk = u.k1 - u.k0;
+                    // L2 prefetch of B, l2_prefetch k-blocks ahead of the loads: keeps
+                    // DRAM busy beyond what the shared-memory ring can hold in flight
+                    const int pf = p.s.l2_prefetch;
+                    auto prefetch_b = [&](int step) {
+                        const int kp = unit_kblock(p.s, u.tile, u.k0, u.k1, step) * BK;
+                        if (!p.b_mn) {
+                            tma_prefetch_l2_2d(&tmB, kp, n0 + rank * (BN / CM));
+                        } else {
 #pragma unroll
-                        for (int c = rank * (BN / 64) / CM; c < (rank + 1) * (BN / 64) / CM; ++c)
-                            tma_prefetch_l2_2d(&tmB, n0 + 64 * c, kp);
-                    }
-                };
-                for (int i = 0; i < pf && i < nk; ++i) prefetch_b(i);
-                for (int i = 0; i < nk; ++i) {
-                    const int kb = unit_kblock(p.s, u.tile, u.k0, u.k1, i);
-                    if (pf > 0 && i + pf < nk) prefetch_b(i + pf);
-                    if (!mbar_wait(empty_bar(stage), phase ^ 1u, p.pipe_limit_ns)) {
-                        fail_pipe();
-                        ok = false;
-                        break;
-                    }
-                    if (*abort_flag) { ok = false; break; }
-                    const uint32_t fb = full_bar(stage);
-                    const uint32_t sa = sbase + stage * Cf::STAGE_BYTES;
-                    const uint32_t sb = sa + Cf::A_STAGE_BYTES;
-                    const int k_el = kb * BK;
-                    if constexpr (PAIR_MMA) {
-                        // both CTAs' copies complete on the first CTA's barrier
-                        const uint32_t fbc = mapa_shared(fb, 0);
-                        if (rank == 0) mbar_arrive_expect_tx(fb, 2 * Cf::STAGE_BYTES);
+                            for (int c = rank * (BN / 64) / CM; c < (rank + 1) * (BN / 64) / CM; ++c)
+                                tma_prefetch_l2_2d(&tmB, n0 + 64 * c, kp);
+                        }
+                    };
+                    for (int i = 0; i < pf && i < nk; ++i) prefetch_b(i);
+                    for (int i = 0; i < nk; ++i) {
+                        const int kb = unit_kblock(p.s, u.tile, u.k0, u.k1, i);
+                        if (pf > 0 && i + pf < nk) prefetch_b(i + pf);
+                        if (!mbar_wait(empty_bar(stage), phase ^ 1u, p.pipe_limit_ns)) {
+                            fail_pipe();
+                            ok = false;
+                            break;
+                        }
+                        if (*abort_flag) { ok = false; break; }
+                        const uint32_t fb = full_bar(stage);
+                        const uint32_t sa = sbase + stage * Cf::STAGE_BYTES;
+                        const uint32_t sb = sa + Cf::A_STAGE_BYTES;
+                        const int k_el = kb * BK;
+                        if constexpr (PAIR_MMA) {
+                            // both CTAs' copies complete on the first CTA's barrier
+                            const uint32_t fbc = mapa_shared(fb, 0);
+                            if (rank == 0) mbar_arrive_expect_tx(fb, 2 * Cf::STAGE_BYTES);
+                            if (!p.a_mn) {
+                                tma_load_2d_pair(sa, &tmA, fbc, k_el, m0, HINT, pol_a);  // AROWS rows
+                            } else {
+#pragma unroll
+                                for (int c = 0; c < AROWS / 64; ++c)
+                                    tma_load_2d_pair(sa + c * MN_CHUNK_BYTES, &tmA, fbc, m0 + 64 * c,
+                                                     k_el, HINT, pol_a);
+                            }
+                            const int nb = n0 + rank * (BN / 2);  // this CTA's half of B
+                            if (!p.b_mn) {
+                                tma_load_2d_pair(sb, &tmB, fbc, k_el, nb, HINT, policy);
+                            } else {
+#pragma unroll
+                                for (int c = 0; c < BN / 128; ++c)
+                                    tma_load_2d_pair(sb + c * MN_CHUNK_BYTES, &tmB, fbc, nb + 64 * c,
+                                                     k_el, HINT, policy);
+                            }
+                        } else {
+                        mbar_arrive_expect_tx(fb, Cf::STAGE_BYTES);
                         if (!p.a_mn) {
-                            tma_load_2d_pair(sa, &tmA, fbc, k_el, m0, pol_a);  // AROWS rows
+                            tma_load_2d(sa, &tmA, fb, k_el, m0, HINT, pol_a);  // box of AROWS rows
                         } else {
 #pragma unroll
                             for (int c = 0; c < AROWS / 64; ++c)
-                                tma_load_2d_pair(sa + c * MN_CHUNK_BYTES, &tmA, fbc, m0 + 64 * c,
-                                                 k_el, pol_a);
+                                tma_load_2d(sa + c * MN_CHUNK_BYTES, &tmA, fb, m0 + 64 * c, k_el, HINT,
+                                            pol_a);
                         }
-                        const int nb = n0 + rank * (BN / 2);  // this CTA's half of B
-                        if (!p.b_mn) {
-                            tma_load_2d_pair(sb, &tmB, fbc, k_el, nb, policy);
+                        if constexpr (CM == 1) {
+                            if (!p.b_mn) {
+                                tma_load_2d(sb, &tmB, fb, k_el, n0, HINT, policy);
+                            } else {
+#pragma unroll
+                                for (int c = 0; c < BN / 64; ++c)
+                                    tma_load_2d(sb + c * MN_CHUNK_BYTES, &tmB, fb, n0 + 64 * c, k_el, HINT,
+                                                policy);
+                            }
                         } else {
+                            // this CTA's half of B, into both CTAs of the pair
+                            if (!p.b_mn) {
+                                const int half = BN / 2;  // rows of the K-major box
+                                tma_load_2d_multicast(sb + rank * half * 128, &tmB, fb, k_el,
+                                                      n0 + rank * half, PAIR_MASK, HINT, policy);
+                            } else {
 #pragma unroll
-                            for (int c = 0; c < BN / 128; ++c)
-                                tma_load_2d_pair(sb + c * MN_CHUNK_BYTES, &tmB, fbc, nb + 64 * c,
-                                                 k_el, policy);
+                                for (int c = rank * (BN / 128); c < (rank + 1) * (BN / 128); ++c)
+                                    tma_load_2d_multicast(sb + c * MN_CHUNK_BYTES, &tmB, fb,
+                                                          n0 + 64 * c, k_el, PAIR_MASK, HINT, policy);
+                            }
                         }
-                    } else {
-                    mbar_arrive_expect_tx(fb, Cf::STAGE_BYTES);
-                    if (!p.a_mn) {
-                        tma_load_2d(sa, &tmA, fb, k_el, m0, pol_a);  // box of AROWS rows
-                    } else {
-#pragma unroll
-                        for (int c = 0; c < AROWS / 64; ++c)
-                            tma_load_2d(sa + c * MN_CHUNK_BYTES, &tmA, fb, m0 + 64 * c, k_el, pol_a);
-                    }
-                    if constexpr (CM == 1) {
-                        if (!p.b_mn) {
-                            tma_load_2d(sb, &tmB, fb, k_el, n0, policy);
-                        } else {
-#pragma unroll
-                            for (int c = 0; c < BN / 64; ++c)
-                                tma_load_2d(sb + c * MN_CHUNK_BYTES, &tmB, fb, n0 + 64 * c, k_el,
-                                            policy);
+                        }  // not a pair MMA
+                        filled |= 1u << stage;
+                        fill_parity = (fill_parity & ~(1u << stage)) | (phase << stage);
+                        if (++stage == STAGES) {
+                            stage = 0;
+                            phase ^= 1u;
                         }
-                    } else {
-                        // this CTA's half of B, into both CTAs of the pair
-                        if (!p.b_mn) {
-                            const int half = BN / 2;  // rows of the K-major box
-                            tma_load_2d_multicast(sb + rank * half * 128, &tmB, fb, k_el,
-                                                  n0 + rank * half, PAIR_MASK, policy);
-                        } else {
-#pragma unroll
-                            for (int c = rank * (BN / 128); c < (rank + 1) * (BN / 128); ++c)
-                                tma_load_2d_multicast(sb + c * MN_CHUNK_BYTES, &tmB, fb,
-                                                      n0 + 64 * c, k_el, PAIR_MASK, policy);
-                        }
-                    }
-                    }  // not a pair MMA
-                    filled |= 1u << stage;
-                    fill_parity = (fill_parity & ~(1u << stage)) | (phase << stage);
-                    if (++stage == STAGES) {
-                        stage = 0;
-                        phase ^= 1u;
                     }
                 }
-            }
+            };
+            if (b_once)
+                produce(BoolConst<true>{});
+            else
+                produce(BoolConst<false>{});
             if (p.trace) p.trace[(size_t)cta * TRACE_N + TRACE_LOADS_DONE] = globaltimer_ns();
             // before the CTA (or its peer) exits: every copy into this CTA has
             // landed, and every MMA that reads this CTA's ring (the peer's too)
