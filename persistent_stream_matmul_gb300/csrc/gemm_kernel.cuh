@@ -514,11 +514,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             uint32_t phase = 0;
             uint32_t filled = 0, fill_parity = 0;  // per-stage bit masks
             bool ok = true;
+            // pair MMA: the first CTA's full barriers, as shared::cluster
+            // addresses (consecutive like the local ones)
+            const uint32_t full0_c = PAIR_MMA ? mapa_shared(full_bar(0), 0) : 0u;
             auto produce = [&](auto hint_tag) {
                 constexpr bool HINT = decltype(hint_tag)::value;
                 while (ok && cursor_next(p.s, unit_cta, cur, u)) {
                     const int m0 = (u.tm * CM + rank) * BM, n0 = u.tn * BN;
                     const int nk = u.k1 - u.k0;
+                    // Per-unit work stays out of the k-loop: whether the unit's
+                    // k-blocks are rotated, and the abort check.  The loop is on
+                    // the ring's critical path (a stage is refilled as soon as
+                    // it is released); with these in it, and the peer barrier
+                    // address recomputed every k-block, the tensor pipe idled
+                    // ~9 % more of its cycles on a large square product.
+                    const bool rot_unit = p.s.k_rotate && u.k0 == 0 && u.k1 == p.s.ipt;
+                    if (*abort_flag) { ok = false; break; }
                     // L2 prefetch of B, l2_prefetch k-blocks ahead of the loads: keeps
                     // DRAM busy beyond what the shared-memory ring can hold in flight
                     const int pf = p.s.l2_prefetch;
@@ -534,21 +545,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     };
                     for (int i = 0; i < pf && i < nk; ++i) prefetch_b(i);
                     for (int i = 0; i < nk; ++i) {
-                        const int kb = unit_kblock(p.s, u.tile, u.k0, u.k1, i);
+                        const int kb = rot_unit ? unit_kblock(p.s, u.tile, u.k0, u.k1, i) : u.k0 + i;
                         if (pf > 0 && i + pf < nk) prefetch_b(i + pf);
                         if (!mbar_wait(empty_bar(stage), phase ^ 1u, p.pipe_limit_ns)) {
                             fail_pipe();
                             ok = false;
                             break;
                         }
-                        if (*abort_flag) { ok = false; break; }
                         const uint32_t fb = full_bar(stage);
                         const uint32_t sa = sbase + stage * Cf::STAGE_BYTES;
                         const uint32_t sb = sa + Cf::A_STAGE_BYTES;
                         const int k_el = kb * BK;
                         if constexpr (PAIR_MMA) {
                             // both CTAs' copies complete on the first CTA's barrier
-                            const uint32_t fbc = mapa_shared(fb, 0);
+                            const uint32_t fbc = full0_c + 8u * (uint32_t)stage;
                             if (rank == 0) mbar_arrive_expect_tx(fb, 2 * Cf::STAGE_BYTES);
                             if (!p.a_mn) {
                                 tma_load_2d_pair(sa, &tmA, fbc, k_el, m0, HINT, pol_a);  // AROWS rows
