@@ -497,7 +497,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
-        if (lane == 0) {
+        // The whole warp runs the loop and takes every branch together (waits
+        // are voted); one elected lane issues the copies.  With the loop run
+        // by lane 0 alone, its values were not warp-uniform and each copy took
+        // ~130 cycles to issue, on the ring's critical path: the warp-wide
+        // form took ~9 % off the SM cycles of a large square product.
+        {
             // With a single row of tiles every B tile is read exactly once:
             // let it leave L2 first and keep the small, shared A resident.
             // Otherwise the copies carry no L2 policy at all (the cache-hint
@@ -529,7 +534,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     // address recomputed every k-block, the tensor pipe idled
                     // ~9 % more of its cycles on a large square product.
                     const bool rot_unit = p.s.k_rotate && u.k0 == 0 && u.k1 == p.s.ipt;
-                    if (*abort_flag) { ok = false; break; }
+                    if (__any_sync(0xffffffffu, *abort_flag != 0)) { ok = false; break; }
                     // L2 prefetch of B, l2_prefetch k-blocks ahead of the loads: keeps
                     // DRAM busy beyond what the shared-memory ring can hold in flight
                     const int pf = p.s.l2_prefetch;
@@ -543,73 +548,78 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                 tma_prefetch_l2_2d(&tmB, n0 + 64 * c, kp);
                         }
                     };
-                    for (int i = 0; i < pf && i < nk; ++i) prefetch_b(i);
+                    if (lane == 0)
+                        for (int i = 0; i < pf && i < nk; ++i) prefetch_b(i);
                     for (int i = 0; i < nk; ++i) {
                         const int kb = rot_unit ? unit_kblock(p.s, u.tile, u.k0, u.k1, i) : u.k0 + i;
-                        if (pf > 0 && i + pf < nk) prefetch_b(i + pf);
-                        if (!mbar_wait(empty_bar(stage), phase ^ 1u, p.pipe_limit_ns)) {
-                            fail_pipe();
+                        if (pf > 0 && i + pf < nk && lane == 0) prefetch_b(i + pf);
+                        if (!__all_sync(0xffffffffu,
+                                        mbar_wait(empty_bar(stage), phase ^ 1u, p.pipe_limit_ns))) {
+                            if (lane == 0) fail_pipe();
                             ok = false;
                             break;
                         }
-                        const uint32_t fb = full_bar(stage);
-                        const uint32_t sa = sbase + stage * Cf::STAGE_BYTES;
-                        const uint32_t sb = sa + Cf::A_STAGE_BYTES;
-                        const int k_el = kb * BK;
-                        if constexpr (PAIR_MMA) {
-                            // both CTAs' copies complete on the first CTA's barrier
-                            const uint32_t fbc = full0_c + 8u * (uint32_t)stage;
-                            if (rank == 0) mbar_arrive_expect_tx(fb, 2 * Cf::STAGE_BYTES);
+                        if (elect_one()) {
+                            const uint32_t fb = full_bar(stage);
+                            const uint32_t sa = sbase + stage * Cf::STAGE_BYTES;
+                            const uint32_t sb = sa + Cf::A_STAGE_BYTES;
+                            const int k_el = kb * BK;
+                            if constexpr (PAIR_MMA) {
+                                // both CTAs' copies complete on the first CTA's barrier
+                                const uint32_t fbc = full0_c + 8u * (uint32_t)stage;
+                                if (rank == 0) mbar_arrive_expect_tx(fb, 2 * Cf::STAGE_BYTES);
+                                if (!p.a_mn) {
+                                    tma_load_2d_pair(sa, &tmA, fbc, k_el, m0, HINT, pol_a);  // AROWS rows
+                                } else {
+#pragma unroll
+                                    for (int c = 0; c < AROWS / 64; ++c)
+                                        tma_load_2d_pair(sa + c * MN_CHUNK_BYTES, &tmA, fbc, m0 + 64 * c,
+                                                         k_el, HINT, pol_a);
+                                }
+                                const int nb = n0 + rank * (BN / 2);  // this CTA's half of B
+                                if (!p.b_mn) {
+                                    tma_load_2d_pair(sb, &tmB, fbc, k_el, nb, HINT, policy);
+                                } else {
+#pragma unroll
+                                    for (int c = 0; c < BN / 128; ++c)
+                                        tma_load_2d_pair(sb + c * MN_CHUNK_BYTES, &tmB, fbc, nb + 64 * c,
+                                                         k_el, HINT, policy);
+                                }
+                            } else {
+                            mbar_arrive_expect_tx(fb, Cf::STAGE_BYTES);
                             if (!p.a_mn) {
-                                tma_load_2d_pair(sa, &tmA, fbc, k_el, m0, HINT, pol_a);  // AROWS rows
+                                tma_load_2d(sa, &tmA, fb, k_el, m0, HINT, pol_a);  // box of AROWS rows
                             } else {
 #pragma unroll
                                 for (int c = 0; c < AROWS / 64; ++c)
-                                    tma_load_2d_pair(sa + c * MN_CHUNK_BYTES, &tmA, fbc, m0 + 64 * c,
-                                                     k_el, HINT, pol_a);
+                                    tma_load_2d(sa + c * MN_CHUNK_BYTES, &tmA, fb, m0 + 64 * c, k_el, HINT,
+                                                pol_a);
                             }
-                            const int nb = n0 + rank * (BN / 2);  // this CTA's half of B
-                            if (!p.b_mn) {
-                                tma_load_2d_pair(sb, &tmB, fbc, k_el, nb, HINT, policy);
+                            if constexpr (CM == 1) {
+                                if (!p.b_mn) {
+                                    tma_load_2d(sb, &tmB, fb, k_el, n0, HINT, policy);
+                                } else {
+#pragma unroll
+                                    for (int c = 0; c < BN / 64; ++c)
+                                        tma_load_2d(sb + c * MN_CHUNK_BYTES, &tmB, fb, n0 + 64 * c, k_el, HINT,
+                                                    policy);
+                                }
                             } else {
+                                // this CTA's half of B, into both CTAs of the pair
+                                if (!p.b_mn) {
+                                    const int half = BN / 2;  // rows of the K-major box
+                                    tma_load_2d_multicast(sb + rank * half * 128, &tmB, fb, k_el,
+                                                          n0 + rank * half, PAIR_MASK, HINT, policy);
+                                } else {
 #pragma unroll
-                                for (int c = 0; c < BN / 128; ++c)
-                                    tma_load_2d_pair(sb + c * MN_CHUNK_BYTES, &tmB, fbc, nb + 64 * c,
-                                                     k_el, HINT, policy);
+                                    for (int c = rank * (BN / 128); c < (rank + 1) * (BN / 128); ++c)
+                                        tma_load_2d_multicast(sb + c * MN_CHUNK_BYTES, &tmB, fb,
+                                                              n0 + 64 * c, k_el, PAIR_MASK, HINT, policy);
+                                }
                             }
-                        } else {
-                        mbar_arrive_expect_tx(fb, Cf::STAGE_BYTES);
-                        if (!p.a_mn) {
-                            tma_load_2d(sa, &tmA, fb, k_el, m0, HINT, pol_a);  // box of AROWS rows
-                        } else {
-#pragma unroll
-                            for (int c = 0; c < AROWS / 64; ++c)
-                                tma_load_2d(sa + c * MN_CHUNK_BYTES, &tmA, fb, m0 + 64 * c, k_el, HINT,
-                                            pol_a);
+                            }  // not a pair MMA
                         }
-                        if constexpr (CM == 1) {
-                            if (!p.b_mn) {
-                                tma_load_2d(sb, &tmB, fb, k_el, n0, HINT, policy);
-                            } else {
-#pragma unroll
-                                for (int c = 0; c < BN / 64; ++c)
-                                    tma_load_2d(sb + c * MN_CHUNK_BYTES, &tmB, fb, n0 + 64 * c, k_el, HINT,
-                                                policy);
-                            }
-                        } else {
-                            // this CTA's half of B, into both CTAs of the pair
-                            if (!p.b_mn) {
-                                const int half = BN / 2;  // rows of the K-major box
-                                tma_load_2d_multicast(sb + rank * half * 128, &tmB, fb, k_el,
-                                                      n0 + rank * half, PAIR_MASK, HINT, policy);
-                            } else {
-#pragma unroll
-                                for (int c = rank * (BN / 128); c < (rank + 1) * (BN / 128); ++c)
-                                    tma_load_2d_multicast(sb + c * MN_CHUNK_BYTES, &tmB, fb,
-                                                          n0 + 64 * c, k_el, PAIR_MASK, HINT, policy);
-                            }
-                        }
-                        }  // not a pair MMA
+                        __syncwarp();
                         filled |= 1u << stage;
                         fill_parity = (fill_parity & ~(1u << stage)) | (phase << stage);
                         if (++stage == STAGES) {
@@ -623,7 +633,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 produce(BoolConst<true>{});
             else
                 produce(BoolConst<false>{});
-            if (p.trace) p.trace[(size_t)cta * TRACE_N + TRACE_LOADS_DONE] = globaltimer_ns();
+            if (p.trace && lane == 0) p.trace[(size_t)cta * TRACE_N + TRACE_LOADS_DONE] = globaltimer_ns();
             // before the CTA (or its peer) exits: every copy into this CTA has
             // landed, and every MMA that reads this CTA's ring (the peer's too)
             // has released it
@@ -639,7 +649,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         // (pair MMA: the first CTA of the pair issues for both)
-        if (lane == 0 && (!PAIR_MMA || rank == 0)) {
+        // The whole warp runs the loop and takes every branch together (waits
+        // are voted); one elected lane issues the MMAs and commits.  Run by
+        // lane 0 alone, the loop's values are not warp-uniform and each
+        // tcgen05 issue costs more: the warp-wide form took ~2 % off the SM
+        // cycles of a large square product, on top of the producer's gain.
+        if (!PAIR_MMA || rank == 0) {
             Cursor cur;
             cursor_init(p.s, unit_cta, cur);
             Unit u;
@@ -665,36 +680,43 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const uint32_t idesc = p.idesc;
             while (ok && cursor_next(p.s, unit_cta, cur, u)) {
                 const int buf = iter & 1;
-                if (!mbar_wait(tempty_bar(buf), ((iter >> 1) & 1u) ^ 1u, p.pipe_limit_ns)) {
-                    fail_pipe();
+                const bool got_t =
+                    __all_sync(0xffffffffu, mbar_wait(tempty_bar(buf), ((iter >> 1) & 1u) ^ 1u, p.pipe_limit_ns));
+                if (!got_t) {
+                    if (lane == 0) fail_pipe();
                     break;
                 }
-                if (*abort_flag) break;
+                if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
                 tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + (uint32_t)(buf * BN);
                 for (int i = 0; i < u.k1 - u.k0; ++i) {
-                    if (!mbar_wait(full_bar(stage), phase, p.pipe_limit_ns)) {
-                        fail_pipe();
+                    if (!__all_sync(0xffffffffu, mbar_wait(full_bar(stage), phase, p.pipe_limit_ns))) {
+                        if (lane == 0) fail_pipe();
                         ok = false;
                         break;
                     }
                     tc_fence_after_sync();
+                    const bool leader = elect_one();
                     const uint64_t off = (uint64_t)((uint32_t)(stage * Cf::STAGE_BYTES) >> 4);
 #pragma unroll
                     for (int kk = 0; kk < BK / UMMA_K; ++kk) {
                         const uint64_t adesc = a_desc0 + off + (uint64_t)kk * a_kstep;
                         const uint64_t bdesc = b_desc0 + off + (uint64_t)kk * b_kstep;
-                        if constexpr (PAIR_MMA)
-                            mma_f16_ss_pair(d_tmem, adesc, bdesc, idesc, (i > 0 || kk > 0) ? 1u : 0u);
-                        else
-                            mma_f16_ss(d_tmem, adesc, bdesc, idesc, (i > 0 || kk > 0) ? 1u : 0u);
+                        const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
+                        if (leader) {
+                            if constexpr (PAIR_MMA)
+                                mma_f16_ss_pair(d_tmem, adesc, bdesc, idesc, acc);
+                            else
+                                mma_f16_ss(d_tmem, adesc, bdesc, idesc, acc);
+                        }
                     }
-                    if constexpr (PAIR_MMA) {
-                        mma_commit_pair_multicast(empty_bar(stage), PAIR_MASK);  // frees both rings
-                    } else if constexpr (CM == 2) {
-                        mma_commit_multicast(empty_bar(stage), PAIR_MASK);  // both halves of B were read
-                    } else {
-                        mma_commit(empty_bar(stage));
+                    if (leader) {
+                        if constexpr (PAIR_MMA)
+                            mma_commit_pair_multicast(empty_bar(stage), PAIR_MASK);  // frees both rings
+                        else if constexpr (CM == 2)
+                            mma_commit_multicast(empty_bar(stage), PAIR_MASK);  // both halves of B were read
+                        else
+                            mma_commit(empty_bar(stage));
                     }
                     if (++stage == STAGES) {
                         stage = 0;
@@ -702,17 +724,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     }
                 }
                 if (!ok) break;
-                if constexpr (PAIR_MMA)
-                    mma_commit_pair_multicast(tfull_bar(buf), PAIR_MASK);  // both halves of D ready
-                else
-                    mma_commit(tfull_bar(buf));
+                if (elect_one()) {
+                    if constexpr (PAIR_MMA)
+                        mma_commit_pair_multicast(tfull_bar(buf), PAIR_MASK);  // both halves of D ready
+                    else
+                        mma_commit(tfull_bar(buf));
+                }
+                __syncwarp();
                 ++iter;
             }
-            // all MMAs this thread issued are complete before TMEM is freed
-            if constexpr (PAIR_MMA)
-                mma_commit_pair_multicast(done_bar, 0x1);
-            else
-                mma_commit(done_bar);
+            // all MMAs the warp issued are complete before TMEM is freed
+            __syncwarp();
+            if (elect_one()) {
+                if constexpr (PAIR_MMA)
+                    mma_commit_pair_multicast(done_bar, 0x1);
+                else
+                    mma_commit(done_bar);
+            }
+            __syncwarp();
             mbar_wait(done_bar, 0, p.pipe_limit_ns);
         }
     } else {

@@ -376,6 +376,18 @@ __host__ __device__ __forceinline__ uint32_t idesc_f16(int bf16, int a_mn, int b
            ((uint32_t)b_mn << 16) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
 }
 
+// True in exactly one lane of a converged warp (the warp must be converged:
+// elect.sync takes the full mask).
+__device__ __forceinline__ bool elect_one() {
+    uint32_t pred;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "elect.sync _|p, 0xffffffff;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(pred));
+    return pred != 0;
+}
+
 // ---------------------------------------------------------------- global memory
 __device__ __forceinline__ uint64_t ld_acquire_u64(const unsigned long long* p) {
     uint64_t v;

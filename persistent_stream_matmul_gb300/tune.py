@@ -23,6 +23,12 @@
   short bursts that alternate between them (the order flips every pair), so
   both see the same drift of the clocks under the power cap; reports the
   median ratio and how many pairs each side won.
+* ``vs_cublas``: one plan against torch.matmul (cuBLAS) on the same bf16
+  operands, in ~100 ms bursts that alternate, with the plan's SM clock and
+  its launch time in SM cycles (the clock settles lower for a kernel that
+  draws more power, so cycles compare kernel efficiency and microseconds
+  compare throughput under the cap).  ``--cublas-only`` runs the cuBLAS
+  launches alone, for a profiler capture of the vendor kernel.
 
 Run as ``python -m persistent_stream_matmul_gb300.tune --help``.  Operands
 are random device data (timing does not depend on the values); correctness
@@ -177,6 +183,78 @@ def paired_compare(M, N, K, base, variant, dtype=B.GEMM_BF16, la=0, lb=1, pairs=
             "variant_faster_pairs": sum(1 for r in ratios if r < 1.0), "pairs": pairs}
 
 
+def vs_cublas(M, N, K, schedule="streamk", options=None, rounds=6, burst_ms=100.0, torch_mod=None):
+    """Long bursts of one plan and of torch.matmul (cuBLAS) on the same bf16
+    operands (A row-major, B column-major), alternating, the order flipping
+    every round.  Each burst lasts about `burst_ms`, long enough for the clocks
+    to settle under the power cap for that kernel; the median launch of its
+    last two thirds is kept.  The plan's launches also carry per-CTA stamps,
+    so its SM clock (%clock64 over %globaltimer) and its launch time in SM
+    cycles are reported beside the times."""
+    import numpy as np
+    import torch as t
+    t = torch_mod or t
+    a = t.randn(M, K, device="cuda").to(t.bfloat16)
+    bt = t.randn(N, K, device="cuda").to(t.bfloat16)  # B column-major: its transpose, row-major
+    c = t.empty(M, N, dtype=t.bfloat16, device="cuda")
+    p = B.Plan(M, N, K, B.GEMM_BF16, 0, 1, schedule, **(options or {}))
+    w = t.zeros(max(1, p.workspace_size), dtype=t.uint8, device="cuda")
+    ctas = p.info("grid")
+    stamps = t.zeros(ctas * B.TRACE_STAMPS, dtype=t.int64, device="cuda")
+    p.set_trace(stamps, stamps.numel() * 8)
+    stream = t.cuda.current_stream()
+    flops = 2.0 * M * N * K
+    arms = {"library": lambda: p.run(a, bt, c, w if p.workspace_size else None, stream),
+            "cublas": lambda: t.matmul(a, bt.t(), out=c)}
+    n = max(20, int(burst_ms * 1e3 / (flops / 1.6e15 * 1e6)))
+
+    def burst(fn):
+        ev = [t.cuda.Event(enable_timing=True) for _ in range(n + 1)]
+        t.cuda.synchronize()
+        ev[0].record(stream)
+        for i in range(n):
+            fn()
+            ev[i + 1].record(stream)
+        t.cuda.synchronize()
+        d = [ev[i].elapsed_time(ev[i + 1]) * 1e3 for i in range(n)]
+        return statistics.median(d[n // 3:])
+
+    times = {"library": [], "cublas": []}
+    mhz = []
+    for r in range(rounds):
+        for arm in (("library", "cublas") if r % 2 == 0 else ("cublas", "library")):
+            times[arm].append(burst(arms[arm]))
+            if arm == "library":
+                s = stamps.cpu().numpy().reshape(ctas, B.TRACE_STAMPS).astype(np.float64)
+                ns, cyc = s[:, 3] - s[:, 0], s[:, 5] - s[:, 4]
+                mhz.append(float(np.median(cyc[ns > 0] / ns[ns > 0])) * 1e3)
+    p.set_trace(None, 0)
+    assert p.last_status(stream) == B.GEMM_OK
+    p.close()
+    lib_us, cub_us = statistics.median(times["library"]), statistics.median(times["cublas"])
+    sm_mhz = statistics.median(mhz)
+    return {"M": M, "N": N, "K": K, "schedule": schedule, "options": options or {},
+            "launches_per_burst": n, "rounds": rounds,
+            "library_us": lib_us, "cublas_us": cub_us,
+            "library_tflops": flops / lib_us / 1e6, "cublas_tflops": flops / cub_us / 1e6,
+            "library_over_cublas": statistics.median(
+                [cb / lb for lb, cb in zip(times["library"], times["cublas"])]),
+            "library_sm_mhz": sm_mhz, "library_kcycles": lib_us * sm_mhz / 1e3}
+
+
+def cublas_only(M, N, K, launches=8, torch_mod=None):
+    """torch.matmul (cuBLAS) launches alone on the operands `vs_cublas` uses,
+    for a profiler capture of the vendor kernel."""
+    import torch as t
+    t = torch_mod or t
+    a = t.randn(M, K, device="cuda").to(t.bfloat16)
+    bt = t.randn(N, K, device="cuda").to(t.bfloat16)
+    c = t.empty(M, N, dtype=t.bfloat16, device="cuda")
+    for _ in range(launches):
+        t.matmul(a, bt.t(), out=c)
+    t.cuda.synchronize()
+
+
 def grid_sweep(M, N, K, dtype=B.GEMM_BF16, la=0, lb=1, seed=123, torch_mod=None):
     import torch as t
     t = torch_mod or t
@@ -296,11 +374,21 @@ def main():
     ap.add_argument("--layout-b", type=int, default=1, help="0 row-major, 1 column-major B")
     ap.add_argument("--skinny", action="store_true",
                     help="time SKINNY_SHAPES (fp16, row-major A and B)")
+    ap.add_argument("--vs-cublas", nargs=3, type=int, metavar=("M", "N", "K"),
+                    help="bf16 plan (--schedule) against torch.matmul in long alternating bursts")
+    ap.add_argument("--schedule", default="streamk", help="schedule for --vs-cublas")
+    ap.add_argument("--cublas-only", nargs=3, type=int, metavar=("M", "N", "K"),
+                    help="eight torch.matmul launches alone (for a profiler capture)")
     ap.add_argument("--out", help="also write every record to this file as JSON lines")
     ap.add_argument("--markdown", help="write the sweeps as markdown tables to this file")
     args = ap.parse_args()
     dtype = B.GEMM_BF16 if args.dtype == "bf16" else B.GEMM_F16
+    if args.cublas_only:
+        cublas_only(*args.cublas_only)
+        return
     B.load()
+    if args.vs_cublas:
+        print(json.dumps(vs_cublas(*args.vs_cublas, schedule=args.schedule)), flush=True)
     if args.compare:
         M, N, K = (int(x) for x in args.compare[:3])
         print(json.dumps(paired_compare(M, N, K, json.loads(args.compare[3]), json.loads(args.compare[4]),
