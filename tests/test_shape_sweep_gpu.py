@@ -42,3 +42,14 @@ def test_sampled_shape(M, N, K):
             assert ok, (M, N, K, name, nbad, worst)
             if law == inputs.INT_LAW:
                 assert np.array_equal(got, ref), (M, N, K, name)
+
+
+def test_vs_cublas_record():
+    """The comparison against torch.matmul runs and reports consistent figures
+    (small product, short bursts: the record's form, not its numbers)."""
+    r = tune.vs_cublas(1024, 1024, 1024, rounds=2, burst_ms=5.0)
+    assert r["library_us"] > 0 and r["cublas_us"] > 0
+    assert abs(r["library_tflops"] - 2.0 * 1024 ** 3 / r["library_us"] / 1e6) < 1e-6
+    assert 200.0 < r["library_sm_mhz"] < 3000.0
+    assert abs(r["library_kcycles"] - r["library_us"] * r["library_sm_mhz"] / 1e3) < 1e-6
+    assert 0.05 < r["library_over_cublas"] < 20.0
