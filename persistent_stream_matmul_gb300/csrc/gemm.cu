@@ -301,13 +301,17 @@ gemm_status_t kcl_shape(const gemm_plan* p, int64_t g, int* bn_out, int64_t* s_o
 gemm_status_t derive(gemm_plan* p) {
     const int64_t tiles_m128 = cdiv64(p->M, BM);
     // cluster split-K: the k-parts of a tile run as one cluster of 1-CTA MMAs.
-    // GEMM_SCHED_AUTO takes it when some choice of it fits one wave: for a
-    // single row of 128-row tiles (a skinny, memory-bound product) always --
-    // in a timed sweep of 45 such shapes (M 16-128, N 1024-16384, K
-    // 1024-16384) it was never slower than Stream-K and up to 2.8x faster --
-    // and for more rows when every part has at least 8 k-blocks: on the
-    // log-sampled shapes where it fits one wave it was 8-43 % faster than
-    // the other schedules with parts of 11-46 k-blocks, 25 % slower with 6.
+    // GEMM_SCHED_AUTO takes it when some choice of it fits one wave:
+    //  * for a single row of 128-row tiles (a skinny, memory-bound product)
+    //    when K has more than 16 k-blocks and the unsplit 128-wide tiles
+    //    would fill under 80 % of the SMs.  In a timed sweep of 45 such
+    //    shapes (M 16-128, N 1024-16384, K 1024-16384) it was never slower
+    //    than Stream-K and up to 2.8x faster; with 16 k-blocks (K = 1024) the
+    //    unsplit tiles ran 10-35 % faster, and with N = 16384 (128 tiles) they
+    //    were level or up to 12 % faster;
+    //  * for more rows when every part has at least 8 k-blocks: on the
+    //    log-sampled shapes where it fits one wave it was 8-43 % faster than
+    //    the other schedules with parts of 11-46 k-blocks, 25 % slower with 6.
     const int64_t g_kcl = p->opt_grid > 0 ? p->opt_grid : p->num_sms;
     bool kcl = p->schedule == GEMM_SCHED_SPLITK && p->opt_split_cluster == 1;
     int kcl_bn = 0;
@@ -320,8 +324,10 @@ gemm_status_t derive(gemm_plan* p) {
         bool fits = false;
         gemm_plan q = *p;
         q.opt_split = 0;  // the split-K part count does not apply to the other schedules
+        const int64_t kblocks = cdiv64(p->K, BK);
+        const bool single_row_ok = kblocks > 16 && cdiv64(p->N, 128) * 5 < 4 * g_kcl;
         if (kcl_shape(&q, g_kcl, &kcl_bn, &kcl_s, &fits) == GEMM_OK && fits &&
-            (tiles_m128 == 1 || cdiv64(p->K, BK) >= 8 * kcl_s))
+            (tiles_m128 == 1 ? single_row_ok : kblocks >= 8 * kcl_s))
             kcl = true;
     }
     // Tile width: 256 when that still gives every SM a tile (compute-bound
@@ -357,8 +363,11 @@ gemm_status_t derive(gemm_plan* p) {
 
     // GEMM_SCHED_AUTO: choose from the shape, after a timed sweep of 30
     // log-sampled shapes and the five workloads on GB300:
-    //  * one row of tiles (skinny, memory-bound) -> Stream-K, whose units
-    //    start at different k and so spread the B stream;
+    //  * one row of tiles (skinny, memory-bound) under one wave -> Stream-K,
+    //    whose units start at different k and so spread the B stream; but
+    //    persistent (unsplit tiles) when K has at most 16 k-blocks or the
+    //    tiles fill 80 % of the SMs (the timed sweep of single-row shapes:
+    //    10-35 % and up to 12 % faster than Stream-K there);
     //  * fewer than 8 k-iterations per unit -> persistent (nothing to split);
     //  * four or more waves of tiles -> the hybrid rule, which removes the
     //    last partial wave, when tiles have at least 64 k-iterations or there
@@ -379,7 +388,8 @@ gemm_status_t derive(gemm_plan* p) {
         int64_t sk_h = tiles % g;
         if (tiles - sk_h > g) sk_h += g;
         if (tiles_m == 1 && tiles < g) {
-            sched = GEMM_SCHED_STREAMK;
+            sched = (ipt <= 16 || tiles * 5 >= 4 * (int64_t)g) ? GEMM_SCHED_PERSISTENT
+                                                               : GEMM_SCHED_STREAMK;
         } else if (tiles * ipt < 8 * (int64_t)g) {
             sched = GEMM_SCHED_PERSISTENT;
         } else if (waves >= 4.0) {

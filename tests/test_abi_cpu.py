@@ -185,15 +185,25 @@ def test_auto_schedule_choices(lib):
 
 
 def test_auto_single_row_of_tiles(lib):
-    # split-K reduced inside clusters when a choice of it fills one wave
+    # split-K reduced inside clusters when a choice of it fills one wave, K
+    # has more than 16 k-blocks and the unsplit 128-wide tiles would fill
+    # under 80 % of the SMs
     for M, N, K, bn, S in ((64, 8192, 8192, 256, 4), (16, 1024, 4096, 128, 8),
-                           (128, 16384, 16384, 256, 2)):
+                           (128, 8192, 16384, 256, 4), (128, 2048, 2048, 128, 8)):
         p = B.Plan(M, N, K, B.GEMM_F16, 0, 0, "auto", offline_sms=152)
         assert p.info("schedule") == B.GEMM_SCHED_SPLITK and p.info("split_k_cluster") == 1
         assert (p.info("tile_n"), p.info("split_k"), p.workspace_size) == (bn, S, 0), (M, N, K)
         p.close()
-    # otherwise Stream-K: one k-block (nothing to split), a forced pair
-    # cluster, or too many tiles for one wave of 2-part clusters
+    # unsplit (persistent) tiles when K has 16 k-blocks or fewer, or when the
+    # tiles already fill 80 % of the SMs (shapes of the timed single-row sweep
+    # where these ran 10-35 % faster than the split)
+    for M, N, K in ((128, 8192, 1024), (64, 4096, 1024), (16, 16384, 1024),
+                    (128, 16384, 4096), (128, 16384, 16384)):
+        p = B.Plan(M, N, K, B.GEMM_F16, 0, 0, "auto", offline_sms=152)
+        assert (p.info("schedule"), p.info("split_k_cluster")) == (B.GEMM_SCHED_PERSISTENT, 0), (M, N, K)
+        p.close()
+    # otherwise no cluster split-K: one k-block (nothing to split), a forced
+    # pair cluster, or too many tiles for one wave of 2-part clusters
     for M, N, K, opts in ((64, 8192, 64, {}), (64, 8192, 8192, {"cluster_m": 2}),
                           (64, 65536, 4096, {})):
         p = B.Plan(M, N, K, B.GEMM_F16, 0, 0, "auto", offline_sms=152, **opts)
