@@ -141,3 +141,28 @@ def test_cluster_splitk_host_pipeline(la, lb):
         assert p.last_status(stream) == B.GEMM_OK
         assert np.array_equal(hC.numpy().view(np.uint16).reshape(M, N), Cref)
     p.close()
+
+
+# AUTO on a single row of 128-row tiles: cluster split-K when K has more than
+# 16 k-blocks and the unsplit tiles fill under 80 % of the SMs, else unsplit
+# persistent tiles.  Every element against the oracle, and bit-exact on
+# integer-valued inputs, for each branch (fp16, A and B row-major, like the
+# skinny workload).
+@pytest.mark.parametrize("M,N,K,want_kc", [(64, 4096, 1024, False), (128, 2048, 1000, False),
+                                           (16, 1024, 4096, True), (100, 3000, 2112, True),
+                                           (64, 16384, 2048, False)])
+def test_auto_single_row_parity(M, N, K, want_kc):
+    dtype = inputs.F16
+    p = B.Plan(M, N, K, dtype, 0, 0, "auto")
+    assert p.info("split_k_cluster") == (1 if want_kc else 0), (M, N, K)
+    if not want_kc:
+        assert p.info("schedule") == B.GEMM_SCHED_PERSISTENT
+    ws = Workspace()
+    A, Bm = inputs.operands(M, N, K, dtype, 0, 0, ("normal", 1.0), ("normal", 1.0), 91)
+    C64, S_abs, _ = oracle.gemm(A, Bm, M, N, K, dtype, 0, 0)
+    ok, worst, nbad = oracle.check(run(p, to_device(A), to_device(Bm), M, N, ws), dtype, C64, S_abs, K)
+    assert ok, (nbad, worst)
+    Ai, Bi = inputs.operands(M, N, K, dtype, 0, 0, inputs.INT_LAW, inputs.INT_LAW, 92)
+    _, _, Cref = oracle.gemm(Ai, Bi, M, N, K, dtype, 0, 0, with_abs=False)
+    assert np.array_equal(run(p, to_device(Ai), to_device(Bi), M, N, ws), Cref)
+    p.close()
