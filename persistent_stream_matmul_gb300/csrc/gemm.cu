@@ -131,6 +131,12 @@ struct gemm_plan {
     const void* tm_b_ptr;
     bool tm_valid;
     CUtensorMap tmA, tmB;
+    // C's tensor map (pair-MMA kernels): for this pointer and row stride;
+    // state 0 unknown, 1 usable, -1 not usable (alignment)
+    const void* tm_c_ptr;
+    int64_t tm_c_ld;
+    int tm_c_state;
+    CUtensorMap tmC;
     const void* flags_cleared_for;
     bool attr_set[40];
     unsigned long long* trace;  // optional per-CTA stamps (caller-owned device buffer)
@@ -511,6 +517,7 @@ gemm_status_t derive(gemm_plan* p) {
         p->ws_bytes = 0;
     }
     p->tm_valid = false;
+    p->tm_c_state = 0;
     return GEMM_OK;
 }
 
@@ -642,6 +649,34 @@ gemm_status_t make_plan(gemm_plan_t* out, int64_t M, int64_t N, int64_t K, int d
     }
     *out = p;
     return GEMM_OK;
+}
+
+// Tensor map of C for the whole-tile stores of the pair-MMA kernels:
+// row-major, dims {N, M}, row stride ldc, boxes of 64 columns x 32 rows with
+// the 128-byte swizzle (the epilogue stages each box in that layout).  It
+// needs a 16-byte aligned C and a row stride that is a multiple of 16 bytes;
+// otherwise (and for the other kernels) C is written with vector stores.
+bool encode_c_map(gemm_plan* p, void* C, int64_t ldc) {
+    if (!p->PAIR || !C) return false;
+    if (p->tm_c_state != 0 && p->tm_c_ptr == C && p->tm_c_ld == ldc) return p->tm_c_state > 0;
+    p->tm_c_ptr = C;
+    p->tm_c_ld = ldc;
+    p->tm_c_state = -1;
+    if (((uintptr_t)C & 15u) || ((ldc * 2) & 15)) return false;
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    const CUtensorMapDataType dt =
+        p->dtype == GEMM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    const cuuint64_t dims[2] = {(cuuint64_t)p->N, (cuuint64_t)p->M};
+    const cuuint64_t strides[1] = {(cuuint64_t)ldc * 2};
+    const cuuint32_t box[2] = {64, 32};
+    const cuuint32_t estr[2] = {1, 1};
+    if (enc(&p->tmC, dt, 2, C, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return false;
+    p->tm_c_state = 1;
+    return true;
 }
 
 gemm_status_t encode_maps(gemm_plan* p, const void* A, const void* B) {
@@ -1162,6 +1197,7 @@ gemm_status_t run_impl(gemm_plan_t p, const void* A, const void* B, void* C, voi
     kp.pipe_limit_ns = 4000000000ull;
     kp.trace = (p->trace && p->trace_bytes >= (size_t)p->ctas * TRACE_N * 8) ? p->trace : nullptr;
     kp.early_prefetch = early_prefetch_of(p);
+    kp.c_tma = encode_c_map(p, C, kp.ldc) ? 1 : 0;
 
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3((unsigned)p->ctas, 1, 1);
@@ -1193,7 +1229,7 @@ gemm_status_t run_impl(gemm_plan_t p, const void* A, const void* B, void* C, voi
     // peer that cannot run in time turns into GEMM_ERR_TIMEOUT, never a hang.
     cfg.attrs = attr;
     cfg.numAttrs = na;
-    void* args[3] = {&p->tmA, &p->tmB, &kp};
+    void* args[4] = {&p->tmA, &p->tmB, &p->tmC, &kp};
     cudaError_t e = cudaLaunchKernelExC(&cfg, fn, args);
     if (e != cudaSuccess) {
         cudaGetLastError();

@@ -88,11 +88,15 @@ struct Cfg {
     // ring of up to 224 KB (the CTA may hold 227 KB; barriers and alignment
     // take the rest): 4 stages at BN=256, 7 at BN=128 or with a pair MMA at
     // BN=256, 9 with half-height A at BN=128, 5 with it at BN=256, at most 12
-    static constexpr int STAGES_FIT = (224 * 1024) / STAGE_BYTES;
+    // Pair-MMA kernels write C through tensor copies from a staging area of
+    // 4 KB per epilogue warp (32 rows x 128 bytes, one 64-column box), placed
+    // after the ring: 16 KB taken from the ring (one stage of 32 KB at BN=256).
+    static constexpr int EPI_STAGE_BYTES = PAIR_MMA ? 4 * 32 * 128 : 0;
+    static constexpr int STAGES_FIT = (224 * 1024 - EPI_STAGE_BYTES) / STAGE_BYTES;
     static constexpr int STAGES = STAGES_FIT > 12 ? 12 : STAGES_FIT;
     static constexpr int TMEM_COLS = 2 * BN;  // two accumulators; 256 or 512
     static constexpr int BAR_BYTES = 256;
-    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + BAR_BYTES + 1024;
+    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + EPI_STAGE_BYTES + BAR_BYTES + 1024;
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
     static_assert(BN == 64 || BN == 128 || BN == 256, "tile width");
     static_assert(AROWS == 128 || AROWS == 64, "rows of A per stage");
@@ -117,6 +121,7 @@ struct KParams {
     uint64_t pipe_limit_ns;      // any wait inside the CTA's own pipeline
     unsigned long long* trace;   // optional: TRACE_N stamps per CTA, or null
     int32_t early_prefetch;      // k-blocks of the first unit brought into L2 before the wait
+    int32_t c_tma;               // 1: whole tiles store C through tensor copies (tmC)
 };
 
 // Per-CTA trace stamps: nanoseconds of %globaltimer at the start of the CTA,
@@ -366,7 +371,7 @@ __device__ __forceinline__ uint32_t pack2(float a, float b) {
 template <int BN, bool OUT_BF16, int CM, int AROWS = 128, bool PAIR_MMA = false, bool KCL = false>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                const __grid_constant__ KParams p) {
+                const __grid_constant__ CUtensorMap tmC, const __grid_constant__ KParams p) {
     using Cf = Cfg<BN, AROWS, PAIR_MMA>;
     static_assert(!PAIR_MMA || CM == 2, "a pair MMA needs a 2-CTA cluster");
     static_assert(AROWS == 128 || CM == 1 || PAIR_MMA, "half-height A: no multicast clusters");
@@ -381,8 +386,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
     const uint32_t sbase = raw + pad;
-    uint8_t* bar_area = smem_raw + pad + STAGES * Cf::STAGE_BYTES;
-    const uint32_t bar_base = sbase + STAGES * Cf::STAGE_BYTES;
+    const uint32_t epi_stage = sbase + STAGES * Cf::STAGE_BYTES;  // C boxes (pair MMA)
+    uint8_t* bar_area = smem_raw + pad + STAGES * Cf::STAGE_BYTES + Cf::EPI_STAGE_BYTES;
+    const uint32_t bar_base = epi_stage + Cf::EPI_STAGE_BYTES;
     auto full_bar = [&](int s) { return bar_base + 8u * s; };
     auto empty_bar = [&](int s) { return bar_base + 8u * (STAGES + s); };
     auto tfull_bar = [&](int b) { return bar_base + 8u * (2 * STAGES + b); };
@@ -958,6 +964,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     }
                 }
                 uint8_t* crow = reinterpret_cast<uint8_t*>(p.C) + ((size_t)row * p.ldc) * 2;
+                // pair MMA, a tile in mid-stream (its ring is busy): C through
+                // tensor copies when the plan has a tensor map for C
+                const bool c_box = Cf::EPI_STAGE_BYTES > 0 && p.c_tma && store && !c_staged;
 #pragma unroll 1
                 for (int j = 0; j < BN / 32; ++j) {
                     uint32_t r[32];
@@ -1015,7 +1024,39 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             }
                         }
                     }
-                    if (store && row_ok) {
+                    if (c_box) {
+                        // Two 32-column chunks make one 64-column box of the warp's
+                        // 32 rows.  It is staged in the warp's own 4 KB, 16-byte units
+                        // XOR-swizzled by row (the layout of a 128-byte-swizzled
+                        // tensor box; conflict-free writes by the row-owning lanes),
+                        // and written by one tensor copy: full 128-byte lines to L2
+                        // instead of 16 bytes in each of 32 rows per store.
+                        const uint32_t stg = epi_stage + (uint32_t)((warp & 3) * 4096);
+                        if ((j & 1) == 0) {
+                            // the previous box's copy has read the buffer
+                            if (lane == 0) bulk_wait_group_read_0();
+                            __syncwarp();
+                        }
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) {
+                            const int unit = ((j & 1) * 4 + v) ^ (lane & 7);
+                            st_shared_u4(stg + (uint32_t)(lane * 128 + unit * 16),
+                                         pack2<OUT_BF16>(acc[8 * v], acc[8 * v + 1]),
+                                         pack2<OUT_BF16>(acc[8 * v + 2], acc[8 * v + 3]),
+                                         pack2<OUT_BF16>(acc[8 * v + 4], acc[8 * v + 5]),
+                                         pack2<OUT_BF16>(acc[8 * v + 6], acc[8 * v + 7]));
+                        }
+                        if (j & 1) {
+                            fence_proxy_async_smem();
+                            __syncwarp();
+                            if (lane == 0) {
+                                const int x = u.tn * BN + (j - 1) * 32;  // multiple of 64
+                                const int y = tm * BM + (warp & 3) * 32;
+                                if (x < p.N && y < p.M) tma_store_2d(&tmC, stg, x, y);
+                                bulk_commit_group();
+                            }
+                        }
+                    } else if (store && row_ok) {
                         if (c_staged) {
                             const uint32_t srow = sbase + (uint32_t)(row_in_tile * BN * 2);
 #pragma unroll
@@ -1070,6 +1111,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }  // not a cluster split-K part
             ++iter;
         }
+        // every tensor copy of C has completed before the CTA ends
+        if (Cf::EPI_STAGE_BYTES > 0 && p.c_tma && lane == 0) bulk_wait_group_0();
     }
 
     tc_fence_before_sync();

@@ -481,6 +481,25 @@ __device__ __forceinline__ void bulk_wait_group_0() {
     asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
+// Wait until every bulk copy this thread committed has finished reading its
+// shared-memory source (the buffer may then be rewritten).
+__device__ __forceinline__ void bulk_wait_group_read_0() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
+// Tensor copy of a box from shared memory to global memory (the box's
+// coordinates x, innermost, and y in elements; parts outside the tensor are
+// not written).  Completion is tracked by the bulk group of the issuing
+// thread (bulk_commit_group / bulk_wait_group_*).
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int32_t x,
+                                             int32_t y) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+            reinterpret_cast<uint64_t>(map)),
+        "r"(src), "r"(x), "r"(y)
+        : "memory");
+}
+
 __device__ __forceinline__ void st_u2(void* p, uint32_t a, uint32_t b) {
     asm volatile("st.global.v2.b32 [%0], {%1, %2};" ::"l"(p), "r"(a), "r"(b) : "memory");
 }
