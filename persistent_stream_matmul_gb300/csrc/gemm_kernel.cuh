@@ -85,12 +85,13 @@ struct Cfg {
     // a pair MMA keeps only this CTA's half of the B tile in its ring
     static constexpr int B_STAGE_BYTES = (PAIR_MMA ? BN / 2 : BN) * BK * 2;
     static constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
-    // ring of up to 224 KB (the CTA may hold 227 KB; barriers and alignment
-    // take the rest): 4 stages at BN=256, 7 at BN=128 or with a pair MMA at
-    // BN=256, 9 with half-height A at BN=128, 5 with it at BN=256, at most 12
-    // Pair-MMA kernels write C through tensor copies from a staging area of
-    // 4 KB per epilogue warp (32 rows x 128 bytes, one 64-column box), placed
-    // after the ring: 16 KB taken from the ring (one stage of 32 KB at BN=256).
+    // Ring of up to 224 KB (the CTA may hold 227 KB; barriers and alignment
+    // take the rest), at most 12 stages.  Pair-MMA kernels also write C
+    // through tensor copies from a staging area of 4 KB per epilogue warp
+    // (32 rows x 128 bytes, one 64-column box) after the ring, taken from the
+    // same budget.  Stages: 4 at BN=256, 7 at BN=128, 9 with half-height A at
+    // BN=128 and 5 with it at BN=256; with a pair MMA, 6 at BN=256 and 8 at
+    // BN=128.
     static constexpr int EPI_STAGE_BYTES = PAIR_MMA ? 4 * 32 * 128 : 0;
     static constexpr int STAGES_FIT = (224 * 1024 - EPI_STAGE_BYTES) / STAGE_BYTES;
     static constexpr int STAGES = STAGES_FIT > 12 ? 12 : STAGES_FIT;
